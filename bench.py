@@ -1,0 +1,447 @@
+#!/usr/bin/env python3
+"""Decode-step attention benchmark on GB300: µs per step and KV-read GB/s.
+
+One step = one fa_decode call (split-K kernel + log-sum-exp merge kernel)
+over every sequence of the workload, inputs resident in HBM.  The headline
+line is measured on the 4-sequence, 16/8-head, head_dim 256, ragged
+1K-8K workload (cfg2); every other decode workload is measured too and
+listed under "configs".
+
+Timing: W untimed warm-up steps, then K timed steps bracketed by a barrier and
+torch.cuda.synchronize() on both sides; each step is timed with CUDA events on
+the launching stream.  When a workload's KV bytes are under 4x the L2 size,
+L2 is flushed (a 512 MiB buffer is written) before every timed step, outside
+its events.  The split kernel's own duration comes from events the library
+records around it (fa_decode_profile_next) on the same stream.
+
+--impl reference times the fp64 CPU oracle on the host cores on a bounded
+sample of the same workload (the reference arm of this benchmark).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode attention µs/step and KV-read GB/s (fraction of GB300 HBM peak)"
+HEADLINE = "cfg2"
+L2_BYTES = 129 * 2 ** 20
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=HEADLINE)
+    ap.add_argument("--only", action="store_true", help="measure only --workload (for profiling)")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+# --------------------------------------------------------------- distributed
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64,
+                     device="cuda" if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# --------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples every 200 ms while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------- our arm
+def prepare(wl, device):
+    import torch
+    from decode_step_kv_gb300 import binding
+    from decode_step_kv_gb300.inputs import make_inputs
+    d = make_inputs(wl, device)
+    if wl.v_int8:
+        vf = d.pop("v_f32")
+        codes = torch.empty(vf.shape, dtype=torch.int8, device=device)
+        scales = torch.empty(vf.shape[:-1] + (wl.head_dim // 32,), dtype=torch.float16,
+                             device=device)
+        binding.fa_quantize_v_int8(vf, codes, scales)
+        del vf
+        d["v_cache"], d["v_scales"] = codes, scales
+    else:
+        d["v_scales"] = None
+    cap = d["max_blocks"] * (wl.page_size if wl.paged else 1)
+    d["workspace"] = binding.alloc_workspace(wl.batch, wl.n_q_heads, wl.n_kv_heads,
+                                             wl.head_dim, cap, device=device)
+    d["out"] = torch.empty((wl.batch, wl.n_q_heads, wl.head_dim), dtype=torch.float32,
+                           device=device)
+    return d
+
+
+def call(wl, d, stream, out=None):
+    from decode_step_kv_gb300 import binding
+    binding.fa_decode(d["q"], d["k_cache"], d["v_cache"], d["v_scales"], d["block_table"],
+                      d["seq_lens"], wl.n_q_heads, wl.n_kv_heads, wl.head_dim, wl.scale,
+                      d["window"], d["out"] if out is None else out, batch=wl.batch,
+                      page_size=wl.page_size, max_blocks_per_seq=d["max_blocks"],
+                      num_blocks=d["num_blocks"] if wl.paged else 0, workspace=d["workspace"],
+                      stream=stream)
+
+
+def time_kernel(wl, d, steps, warmup, world, device, clocks_gpu=None):
+    """Kernel-only timing.  Returns dict with per-step and split-kernel µs."""
+    import torch
+    from decode_step_kv_gb300 import binding
+    from decode_step_kv_gb300.inputs import kv_bytes
+    nbytes = kv_bytes(wl, d["lens"], None if d["window"] is None else d["window"].tolist())
+    flush = None
+    if nbytes < 4 * L2_BYTES:
+        flush = torch.empty(512 * 2 ** 20, dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream(device)
+    for _ in range(warmup):
+        if flush is not None:
+            flush.fill_(1)
+        call(wl, d, stream)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    sampler = ClockSampler(clocks_gpu) if clocks_gpu is not None else None
+    barrier(world)
+    torch.cuda.synchronize(device)
+    if sampler:
+        sampler.__enter__()
+    t0 = time.perf_counter()
+    for i in range(steps):
+        if flush is not None:
+            flush.fill_(i & 0xFF)
+        ev[i][0].record(stream)
+        binding.fa_decode_profile_next(None, ev[i][1])
+        call(wl, d, stream)
+        ev[i][2].record(stream)
+    torch.cuda.synchronize(device)
+    wall = time.perf_counter() - t0
+    barrier(world)
+    if sampler:
+        sampler.__exit__()
+    step_ms = [a.elapsed_time(c) for a, _, c in ev]
+    split_ms = [a.elapsed_time(b) for a, b, _ in ev]
+    res = {
+        "us_per_step": 1e3 * statistics.mean(step_ms),
+        "us_per_step_median": 1e3 * statistics.median(step_ms),
+        "split_us": 1e3 * statistics.mean(split_ms),
+        "kv_bytes": nbytes,
+        "wall_s": wall,
+        "l2": ("flushed: 512 MiB written before each step" if flush is not None
+               else "inputs larger than 4x L2"),
+        "launches": 2 * steps,
+    }
+    if sampler:
+        res["clocks"] = sampler.summary()
+    return res
+
+
+def time_e2e(wl, d, steps, warmup, device):
+    """Same step through the public API with host inputs: pinned host -> device
+    copies of every input, fa_decode, device -> host copy of the output."""
+    import torch
+    names = ["q", "k_cache", "v_cache", "v_scales", "block_table", "seq_lens", "window"]
+    host = {n: d[n].cpu().pin_memory() for n in names if d.get(n) is not None}
+    dev = {n: torch.empty_like(d[n]) for n in host}
+    out_h = torch.empty(d["out"].shape, dtype=torch.float32).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_h.numel() * 4
+    stream = torch.cuda.current_stream(device)
+    dd = dict(d)
+
+    def step():
+        for n in host:
+            dev[n].copy_(host[n], non_blocking=True)
+        dd.update(dev)
+        call(wl, dd, stream)
+        out_h.copy_(dd["out"], non_blocking=True)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize(device)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    for i in range(steps):
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize(device)
+    ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    return ms, h2d, d2h
+
+
+# --------------------------------------------------------------- CPU oracle
+def oracle_sample(wl, inp, budget_s, threads=0):
+    """Time the oracle on whole (sequence, kv-head) units of the workload until
+    about `budget_s` of CPU work; returns (GB/s, seconds, units, threads)."""
+    import oracle
+    from decode_step_kv_gb300.inputs import attended_tokens
+    lens = inp["lens"]
+    win = None if inp["window"] is None else inp["window"].tolist()
+    toks = attended_tokens(lens, win)
+    G = wl.group
+    vrow = wl.head_dim * (1 if wl.v_int8 else 2) + (wl.head_dim // 32 * 2 if wl.v_int8 else 0)
+    unit_bytes = [t * (2 * wl.head_dim + vrow) for t in toks]
+    n_threads = threads if threads > 0 else (os.cpu_count() or 1)
+    n_units = wl.batch * wl.n_kv_heads
+    per_call = max(1, -(-n_threads // G))       # enough rows to keep every core busy
+    done_bytes, elapsed, units, start, used = 0, 0.0, 0, 0, 1
+    while elapsed < budget_s and units < 4 * n_units:
+        chunk = [(start + i) % n_units for i in range(per_call)]
+        start += per_call
+        rows = []
+        for u in chunk:
+            b, kv = divmod(u, wl.n_kv_heads)
+            rows += [b * wl.n_q_heads + kv * G + g for g in range(G)]
+        used = max(used, min(n_threads, len(rows)))
+        t0 = time.perf_counter()
+        oracle.decode(inp["q"].numpy(), inp["k_cache"].numpy(), inp["v_cache"].numpy(), lens,
+                      scale=wl.scale, n_kv_heads=wl.n_kv_heads,
+                      v_scales=None if inp.get("v_scales") is None else inp["v_scales"].numpy(),
+                      block_table=None if inp["block_table"] is None
+                      else inp["block_table"].numpy(),
+                      window=None if inp["window"] is None else inp["window"].numpy(),
+                      page_size=wl.page_size, max_blocks=inp["max_blocks"], rows=rows,
+                      threads=n_threads)
+        elapsed += time.perf_counter() - t0
+        done_bytes += sum(unit_bytes[u // wl.n_kv_heads] for u in chunk)
+        units += len(chunk)
+    return done_bytes / elapsed / 1e9, elapsed, units, used
+
+
+def cpu_inputs(wl):
+    import torch
+    from decode_step_kv_gb300.inputs import make_inputs
+    inp = make_inputs(wl, "cpu")
+    if wl.v_int8:
+        import oracle
+        c, s = oracle.pack_v_int8(inp.pop("v_f32").numpy())
+        inp["v_cache"] = torch.from_numpy(c)
+        inp["v_scales"] = torch.from_numpy(s.copy())
+    else:
+        inp["v_scales"] = None
+    return inp
+
+
+# --------------------------------------------------------------- arms
+def run_ours(args, world, rank, local):
+    import torch
+    from decode_step_kv_gb300 import binding
+    from decode_step_kv_gb300.inputs import WORKLOADS, WORKLOAD_DESCRIPTIONS
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    binding.load()
+    peak, peak_kind = measured_peaks()
+    wl = WORKLOADS[args.workload]
+    d = prepare(wl, device)
+    gpu_index = int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[0]) \
+        if os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")[0].isdigit() else local
+    r = time_kernel(wl, d, args.steps, args.warmup, world, device, clocks_gpu=gpu_index)
+    us = max_over_ranks(r["us_per_step"], world)
+    split_us = max_over_ranks(r["split_us"], world)
+    gbs_total = world * r["kv_bytes"] / (us * 1e-6) / 1e9
+    achieved = r["kv_bytes"] / (split_us * 1e-6) / 1e9
+    line = {
+        "metric": METRIC,
+        "value": round(gbs_total, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(us / 1e3, 6),
+        "us_per_step": round(us, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic (seeded N(0,1) fp16 q/K/V, random block tables)",
+        "config": {"workload": f"{wl.name}: {WORKLOAD_DESCRIPTIONS[wl.name]}",
+                   "batch": wl.batch, "n_q_heads": wl.n_q_heads, "n_kv_heads": wl.n_kv_heads,
+                   "head_dim": wl.head_dim, "kv_bytes_per_step": r["kv_bytes"],
+                   "l2": r["l2"], "parallelism": f"replicas x{world} (no collectives)"},
+        "frac_of_hbm_peak": round(gbs_total / world / peak, 4),
+        "roofline": {"bound": "hbm", "kernel": "fa_split_kernel",
+                     "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                     "peak_kind": peak_kind, "frac": round(achieved / peak, 4),
+                     "traffic": None},
+        "gpu_launches": r["launches"],
+        "clocks": r.get("clocks"),
+    }
+    if not args.no_e2e:
+        ms, h2d, d2h = time_e2e(wl, d, max(5, args.steps // 5), 2, device)
+        line["e2e"] = {"value": round(r["kv_bytes"] / (ms * 1e-3) / 1e9 * world, 2),
+                       "unit": "GB/s", "us_per_step": round(ms * 1e3, 2),
+                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+    del d
+    torch.cuda.empty_cache()
+    if not args.only:
+        per = {}
+        for name, other in WORKLOADS.items():
+            dd = prepare(other, device)
+            rr = time_kernel(other, dd, max(10, min(args.steps, 30)), 3, world, device)
+            gbs = rr["kv_bytes"] / (rr["us_per_step"] * 1e-6) / 1e9
+            per[name] = {"us_per_step": round(rr["us_per_step"], 2),
+                         "split_us": round(rr["split_us"], 2),
+                         "kv_bytes": rr["kv_bytes"], "GB/s": round(gbs, 1),
+                         "frac_of_peak": round(gbs / peak, 4),
+                         "split_frac_of_peak": round(rr["kv_bytes"] / (rr["split_us"] * 1e-6)
+                                                     / 1e9 / peak, 4),
+                         "l2": rr["l2"]}
+            del dd
+            torch.cuda.empty_cache()
+        line["configs"] = per
+    if rank == 0 and world == 1 and not args.no_cpu:
+        inp = cpu_inputs(wl)
+        gbs, secs, units, thr = oracle_sample(wl, inp, budget_s=12.0)
+        line["cpu_baseline"] = {"value": round(gbs, 4), "unit": "GB/s", "cores": thr,
+                                "kind": "oracle",
+                                "sample": f"{units} (sequence, kv-head) units of {wl.name}, "
+                                          f"all query heads of each, {secs:.1f} s"}
+    if rank == 0:
+        print(json.dumps(line))
+
+
+def run_reference(args, world, rank):
+    """The fp64 CPU oracle, as it stands, on the host cores."""
+    if rank != 0:
+        return
+    from decode_step_kv_gb300.inputs import WORKLOADS, WORKLOAD_DESCRIPTIONS
+    wl = WORKLOADS[args.workload]
+    inp = cpu_inputs(wl)
+    per_step_budget = max(0.2, 150.0 / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        oracle_sample(wl, inp, budget_s=per_step_budget)
+    vals, secs = [], 0.0
+    for _ in range(args.steps):
+        gbs, s, units, thr = oracle_sample(wl, inp, budget_s=per_step_budget)
+        vals.append(gbs)
+        secs += s
+    v = statistics.mean(vals)
+    line = {"impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": "GB/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": None, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": f"{wl.name}: {WORKLOAD_DESCRIPTIONS[wl.name]}"},
+            "cpu_baseline": {"kind": "oracle", "cores": thr, "value": round(v, 4),
+                             "unit": "GB/s",
+                             "sample": f"per step: whole (sequence, kv-head) units of {wl.name} "
+                                       f"for ~{per_step_budget:.1f} s"},
+            "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+def main():
+    args = parse_args()
+    world, rank, local = dist_setup(args)
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_ours(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

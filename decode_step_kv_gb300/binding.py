@@ -1,0 +1,144 @@
+"""Thin Python binding of the C-ABI library (argument marshalling only).
+
+Every function here forwards torch tensors' device pointers to the same-named
+``extern "C"`` entry point of ``libfa_decode.so`` (declared in
+``include/fa_decode.h``); all arithmetic runs in the CUDA kernels.  There is
+no fallback: if the library cannot be built or loaded, the first call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import threading
+from typing import Optional
+
+import torch
+
+from . import _build
+
+_lock = threading.Lock()
+_lib = None
+
+FA_STATUS_LEN_CLAMPED = 1
+FA_STATUS_BAD_BLOCK = 2
+FA_STATUS_WAIT_TIMEOUT = 4
+
+
+class FaDecodeError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"[{code}] {msg}")
+        self.code = code
+
+
+def load(build_if_missing: bool = True) -> ctypes.CDLL:
+    """Load (building first if needed) the CUDA library."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.build() if build_if_missing else _build.LIB
+            lib = ctypes.CDLL(path)
+            P, i32, i64, f32, sz = (ctypes.c_void_p, ctypes.c_int, ctypes.c_longlong,
+                                    ctypes.c_float, ctypes.c_size_t)
+            lib.fa_decode.argtypes = [P, P, P, P, P, P, i32, i32, i32, f32, P, P, i32, i32, i32,
+                                      i32, P, sz, P]
+            lib.fa_decode.restype = i32
+            lib.fa_decode_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32]
+            lib.fa_decode_workspace_size.restype = sz
+            lib.fa_quantize_v_int8.argtypes = [P, i64, i32, P, P, P]
+            lib.fa_quantize_v_int8.restype = i32
+            lib.fa_gather_kv_debug.argtypes = [P, i32, P, i32, i32, i32, i32, i32, i32, P, P]
+            lib.fa_gather_kv_debug.restype = i32
+            lib.fa_decode_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint), P]
+            lib.fa_decode_device_status.restype = i32
+            lib.fa_decode_profile_next.argtypes = [P, P]
+            lib.fa_decode_profile_next.restype = i32
+            lib.fa_decode_last_error.argtypes = []
+            lib.fa_decode_last_error.restype = ctypes.c_char_p
+            _lib = lib
+    return _lib
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("fa_decode takes device tensors")
+    if not t.is_contiguous():
+        raise ValueError("fa_decode takes contiguous tensors")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(rc: int):
+    if rc != 0:
+        raise FaDecodeError(rc, load().fa_decode_last_error().decode())
+
+
+def fa_decode_workspace_size(batch: int, n_q_heads: int, n_kv_heads: int, head_dim: int,
+                             max_kv_len: int, num_sms: int = 0) -> int:
+    return int(load().fa_decode_workspace_size(batch, n_q_heads, n_kv_heads, head_dim,
+                                               max_kv_len, num_sms))
+
+
+def fa_decode(q, k_cache, v_cache, v_scales, block_table, seq_lens, n_q_heads, n_kv_heads,
+              head_dim, scale, window, out, *, batch=None, page_size=16,
+              max_blocks_per_seq=None, num_blocks=None, workspace=None, stream=None):
+    """One decode step: out[b,h] = softmax(scale q.K^T) V over the attended range.
+
+    Layouts and rules are those of ``fa_decode`` in include/fa_decode.h.
+    `batch` defaults to q.shape[0]; `max_blocks_per_seq` to the block table's
+    row length (paged) or k_cache.shape[2] (contiguous); `num_blocks` to
+    k_cache.shape[0] (paged).
+    """
+    if batch is None:
+        batch = q.shape[0]
+    if max_blocks_per_seq is None:
+        max_blocks_per_seq = block_table.shape[1] if block_table is not None else k_cache.shape[2]
+    if num_blocks is None:
+        num_blocks = k_cache.shape[0] if block_table is not None else 0
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = load().fa_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(v_scales),
+                          _ptr(block_table), _ptr(seq_lens), int(n_q_heads), int(n_kv_heads),
+                          int(head_dim), float(scale), _ptr(window), _ptr(out), int(batch),
+                          int(page_size), int(max_blocks_per_seq), int(num_blocks),
+                          _ptr(workspace), ws_bytes, _stream(stream))
+    _check(rc)
+
+
+def fa_quantize_v_int8(x, codes, scales, *, stream=None):
+    """Pack fp32 x [..., D] into int8 codes [..., D] and fp16 scales [..., D/32]."""
+    D = x.shape[-1]
+    rc = load().fa_quantize_v_int8(_ptr(x), x.numel() // D, D, _ptr(codes), _ptr(scales),
+                                   _stream(stream))
+    _check(rc)
+
+
+def fa_gather_kv_debug(cache, row_bytes, block_table, b, n_kv_heads, page_size,
+                       max_blocks_per_seq, num_blocks, n_tokens, dense, *, stream=None):
+    rc = load().fa_gather_kv_debug(_ptr(cache), int(row_bytes), _ptr(block_table), int(b),
+                                   int(n_kv_heads), int(page_size), int(max_blocks_per_seq),
+                                   int(num_blocks), int(n_tokens), _ptr(dense), _stream(stream))
+    _check(rc)
+
+
+def fa_decode_profile_next(split_start=None, split_end=None):
+    """Record torch.cuda.Event objects around the next call's split kernel."""
+    a = None if split_start is None else ctypes.c_void_p(split_start.cuda_event)
+    b = None if split_end is None else ctypes.c_void_p(split_end.cuda_event)
+    _check(load().fa_decode_profile_next(a, b))
+
+
+def fa_decode_device_status(*, stream=None) -> int:
+    v = ctypes.c_uint(0)
+    _check(load().fa_decode_device_status(ctypes.byref(v), _stream(stream)))
+    return int(v.value)
+
+
+def alloc_workspace(batch, n_q_heads, n_kv_heads, head_dim, max_kv_len, device="cuda"):
+    """Device scratch for fa_decode (torch allocation: plumbing, not compute)."""
+    n = fa_decode_workspace_size(batch, n_q_heads, n_kv_heads, head_dim, max_kv_len)
+    return torch.empty(max(n, 16), dtype=torch.uint8, device=device)

@@ -1,0 +1,1062 @@
+// fa_decode.cu -- decode-step (single-query) attention over a paged or
+// contiguous KV cache, for sm_103a (GB300).
+//
+// Structure (one launch pair per decode step):
+//   fa_split_kernel  grid (split, kv_head x head_group, sequence).  Each CTA
+//                    owns one split of one sequence's attended key range for
+//                    one KV head and the query heads that share it (GQA).
+//                    NWARPS warps each stream their own tiles (16 tokens at
+//                    head_dim 128, 8 at 256) of K and V into a private ring of
+//                    shared-memory stages with cp.async.bulk (the TMA engine's
+//                    bulk copy) completing on an mbarrier, then run the QK dot,
+//                    the online softmax and the PV accumulate in fp32.  The
+//                    warps' (O, m, l) are merged in shared memory; a sequence
+//                    with one split writes the normalised output directly,
+//                    otherwise the CTA writes an unnormalised partial.
+//   fa_merge_kernel  one CTA per (sequence, query head): log-sum-exp merge of
+//                    the partials, or the zero row of an empty range.
+//
+// The method follows the mlx-native page "flash_attn_vec_hybrid.metal":
+// chunked KV walk with split-K stride, online softmax (running M, S and the
+// rescale of O), the cross-simdgroup merge, and the NWG > 1 partial layout
+// reduced by a separate pass; the tessl page "nn.rs" (flash_attn_decode) for
+// the two-pass FlashDecoding split sized from the fixed capacity, with both
+// passes deriving the same live split count from the device-side length so
+// the scratch needs no zero fill.  Scores are kept in the base-2 domain
+// (scale * log2 e folded into one multiplier), which changes no result.
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdarg.h>
+#include <stdint.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "../../include/fa_decode.h"
+
+namespace fa {
+
+constexpr int NWARPS = 4;             // consumer warps per CTA (each its own ring)
+constexpr int STAGES = 3;             // shared-memory stages per warp
+constexpr int STAGE_BYTES = 8192;     // one tile of K + V (+ scales)
+constexpr int THREADS = NWARPS * 32;
+constexpr unsigned long long WAIT_NS = 1000000000ull;  // ~1 s bound on any wait
+
+__device__ unsigned int g_status;
+
+// --------------------------------------------------------------- tile geometry
+template <int D, bool VI8>
+struct Geo {
+    static constexpr int TILE = 2048 / D;      // tokens per tile: 16 (D=128), 8 (D=256)
+    static constexpr int KH = TILE / 2;        // keys per half-warp
+    static constexpr int NCH = D / 128;        // 8-element chunks per lane
+    static constexpr int EPL = 8 * NCH;        // head_dim elements per lane
+    static constexpr int K_BYTES = TILE * D * 2;
+    static constexpr int V_ROW = VI8 ? D : 2 * D;
+    static constexpr int V_BYTES = TILE * V_ROW;
+    static constexpr int S_ROW = VI8 ? (D / 32) * 2 : 0;
+    static constexpr int S_BYTES = TILE * S_ROW;
+    static_assert(K_BYTES + V_BYTES + S_BYTES <= STAGE_BYTES, "stage overflow");
+    static_assert((K_BYTES % 16) == 0 && (V_BYTES % 16) == 0 && (S_BYTES % 16) == 0, "align");
+};
+
+struct Params {
+    const __half *q;
+    const char *k;
+    const char *v;
+    const char *vs;
+    const int *bt;
+    const int *seq_lens;
+    const int *window;
+    float *out;
+    float *ws_o;      // [B*Hq][max_splits][D]
+    float2 *ws_ml;    // [B*Hq][max_splits] (m, l), m in log2 units
+    int B, Hq, Hkv, G, n_hg, hpg;
+    int page_size, max_blocks, num_blocks;
+    long long cap;    // tokens per sequence
+    float c2;         // scale * log2(e)
+    int tps;          // tiles per split
+    int max_splits;
+};
+
+// ------------------------------------------------------------ PTX wrappers
+__device__ __forceinline__ uint32_t smem_u32(const void *p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, unsigned count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ unsigned long long global_ns()
+{
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Warp-uniform bounded wait on a stage's phase.  Returns false after ~1 s.
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity)
+{
+    if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity)))
+        return true;
+    const unsigned long long t0 = global_ns();
+    for (;;) {
+        for (int i = 0; i < 256; ++i)
+            if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity)))
+                return true;
+        if (global_ns() - t0 > WAIT_NS)
+            return false;
+    }
+}
+
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes,
+                                         uint32_t bar, uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1], %2, [%3], %4;" ::"r"(dst),
+        "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ uint64_t evict_first_policy()
+{
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+__device__ __forceinline__ float ex2(float x)
+{
+    float y;
+    asm("ex2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ void flag(unsigned bit)
+{
+    atomicOr(&g_status, bit);
+}
+
+// --------------------------------------------------------- range and paging
+// Attended key range [lo, hi) of sequence b (length clamped to capacity).
+__device__ __forceinline__ void attended_range(const Params &p, int b, int &lo, int &hi,
+                                               bool report)
+{
+    long long L = p.seq_lens[b];
+    if (L < 0 || L > p.cap) {
+        if (report)
+            flag(FA_STATUS_LEN_CLAMPED);
+        L = L < 0 ? 0 : p.cap;
+    }
+    const int W = p.window ? p.window[b] : 0;
+    hi = static_cast<int>(L);
+    lo = (W > 0 && hi > W) ? hi - W : 0;
+}
+
+template <int TILE>
+__device__ __forceinline__ int tiles_in(int lo, int hi)
+{
+    return hi > lo ? (hi - 1) / TILE - lo / TILE + 1 : 0;
+}
+
+// Byte offset of token `tok` (a tile start) of (b, kv) in a cache whose rows
+// hold `row_bytes`; -1 when the block id is out of range.
+__device__ __forceinline__ long long row_offset(const Params &p, int b, int kv, int tok,
+                                                int row_bytes)
+{
+    if (p.bt) {
+        const long long blk = p.bt[(long long)b * p.max_blocks + tok / p.page_size];
+        if (blk < 0 || blk >= p.num_blocks)
+            return -1;
+        return ((blk * p.Hkv + kv) * p.page_size + tok % p.page_size) * (long long)row_bytes;
+    }
+    return (((long long)b * p.Hkv + kv) * p.cap + tok) * (long long)row_bytes;
+}
+
+// ------------------------------------------------------------- reductions
+// Transpose-reduce across the 16 lanes of a half-warp: each lane starts with
+// NV partial sums (index = key * GP + head); afterwards lane li holds the
+// complete sums of indices li*NV/16 .. (li+1)*NV/16 - 1 (NV >= 16) or of
+// index li >> (4 - log2 NV) (NV < 16).
+template <int NV, int STEP>
+struct HalfWarpReduce {
+    __device__ __forceinline__ static void run(float *v, int li)
+    {
+        if constexpr (STEP < 4) {
+            constexpr int mask = 8 >> STEP;
+            constexpr int n = NV >> STEP;          // values still held
+            if constexpr (n > 1) {
+                constexpr int h = n / 2;
+                const bool upper = (li & mask) != 0;
+#pragma unroll
+                for (int i = 0; i < h; ++i) {
+                    const float send = upper ? v[i] : v[i + h];
+                    const float keep = upper ? v[i + h] : v[i];
+                    v[i] = keep + __shfl_xor_sync(0xffffffffu, send, mask);
+                }
+            } else {
+                v[0] += __shfl_xor_sync(0xffffffffu, v[0], mask);
+            }
+            HalfWarpReduce<NV, STEP + 1>::run(v, li);
+        }
+    }
+};
+
+template <int NV>
+__device__ __forceinline__ int reduced_index(int li, int r)
+{
+    if constexpr (NV >= 16) {
+        return li * (NV / 16) + r;
+    } else {
+        constexpr int lg = NV >= 8 ? 3 : NV >= 4 ? 2 : NV >= 2 ? 1 : 0;
+        return li >> (4 - lg);
+    }
+}
+
+__device__ __forceinline__ void half8_to_float(const uint4 &raw, float *f)
+{
+    const __half2 *h = reinterpret_cast<const __half2 *>(&raw);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 x = __half22float2(h[i]);
+        f[2 * i] = x.x;
+        f[2 * i + 1] = x.y;
+    }
+}
+
+// ---------------------------------------------------------------- split kernel
+template <int D, int GP, bool VI8>
+__global__ void __launch_bounds__(THREADS, 2) fa_split_kernel(const Params p)
+{
+    using Gm = Geo<D, VI8>;
+    constexpr int TILE = Gm::TILE, KH = Gm::KH, NCH = Gm::NCH, EPL = Gm::EPL;
+    constexpr int NV = KH * GP;
+    constexpr int NVL = NV >= 16 ? NV / 16 : 1;
+    constexpr int NSC = TILE * GP;                 // scores per tile
+    constexpr int NR = (NSC + 31) / 32;            // scores per lane in the softmax step
+
+    const int z = blockIdx.x;
+    const int kv = blockIdx.y / p.n_hg;
+    const int hg = blockIdx.y % p.n_hg;
+    const int b = blockIdx.z;
+
+    int lo, hi;
+    attended_range(p, b, lo, hi, z == 0 && blockIdx.y == 0 && threadIdx.x == 0);
+    const int nt = tiles_in<TILE>(lo, hi);
+    const int n_splits = (nt + p.tps - 1) / p.tps;
+    if (z >= n_splits)
+        return;                                    // capacity-only split: nothing to do
+    const int t_first = lo / TILE + z * p.tps;     // absolute tile index
+    const int t_count = min(p.tps, nt - z * p.tps);
+
+    extern __shared__ __align__(128) unsigned char smem[];
+    unsigned char *stages = smem;
+    float *sbuf_all = reinterpret_cast<float *>(smem + NWARPS * STAGES * STAGE_BYTES);
+    float *mw = sbuf_all + NWARPS * NSC;           // [NWARPS][GP] running max
+    float *lw = mw + NWARPS * GP;                  // [NWARPS][GP] sums
+    float *ow = lw + NWARPS * GP;                  // [NWARPS][GP][D] partial O
+    uint64_t *bars = reinterpret_cast<uint64_t *>(ow + NWARPS * GP * D);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int hw = lane >> 4;
+    const int li = lane & 15;
+    float *sbuf = sbuf_all + warp * NSC;
+    unsigned char *my_stages = stages + warp * STAGES * STAGE_BYTES;
+    const uint32_t my_bars = smem_u32(bars + warp * STAGES);
+
+    if (lane == 0)
+        for (int s = 0; s < STAGES; ++s)
+            mbar_init(my_bars + 8 * s, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    __syncwarp();
+
+    // ---- query heads of this CTA, in registers (fp32), lane's 8-element chunks
+    float qf[GP][EPL];
+#pragma unroll
+    for (int g = 0; g < GP; ++g) {
+        const int gi = hg * p.hpg + g;
+        const bool live = g < p.hpg && gi < p.G;
+        const __half *qrow = p.q + ((long long)b * p.Hq + kv * p.G + gi) * D;
+#pragma unroll
+        for (int c = 0; c < NCH; ++c) {
+            uint4 raw = make_uint4(0, 0, 0, 0);
+            if (live)
+                raw = *reinterpret_cast<const uint4 *>(qrow + c * 128 + li * 8);
+            half8_to_float(raw, &qf[g][c * 8]);
+        }
+    }
+
+    float acc[GP][EPL];
+    float m_run[GP];
+#pragma unroll
+    for (int g = 0; g < GP; ++g) {
+        m_run[g] = -INFINITY;
+#pragma unroll
+        for (int e = 0; e < EPL; ++e)
+            acc[g][e] = 0.f;
+    }
+    float m_mine = -INFINITY;   // running max of head (lane % GP)
+    float l_lane = 0.f;         // this lane's share of the sum for head (lane % GP)
+
+    const uint64_t policy = evict_first_policy();
+    // tiles of this warp: j-th is t_first + warp + j*NWARPS
+    const int n_my = t_count > warp ? (t_count - warp + NWARPS - 1) / NWARPS : 0;
+
+    auto tile_rows = [&](int ti, int &r0, int &r1) {
+        const int base = ti * TILE;
+        r0 = max(lo - base, 0);
+        r1 = min(hi - base, TILE);
+    };
+
+    // Issue the copies of the warp's j-th tile into stage s (lane 0 only).
+    auto issue = [&](int j, int s) {
+        const int ti = t_first + warp + j * NWARPS;
+        int r0, r1;
+        tile_rows(ti, r0, r1);
+        const int tok = ti * TILE;
+        const uint32_t bar = my_bars + 8 * s;
+        unsigned char *st = my_stages + s * STAGE_BYTES;
+        const long long ko = row_offset(p, b, kv, tok, 2 * D);
+        if (ko < 0) {
+            flag(FA_STATUS_BAD_BLOCK);
+            mbar_expect_tx(bar, 0);   // plain arrival: the phase completes with no data
+            return;
+        }
+        const long long vo = row_offset(p, b, kv, tok, Gm::V_ROW);
+        const uint32_t kbytes = (r1 - r0) * 2 * D;
+        const uint32_t vbytes = (r1 - r0) * Gm::V_ROW;
+        uint32_t total = kbytes + vbytes + Gm::S_BYTES;
+        mbar_expect_tx(bar, total);
+        bulk_g2s(smem_u32(st + r0 * 2 * D), p.k + ko + r0 * 2 * D, kbytes, bar, policy);
+        bulk_g2s(smem_u32(st + Gm::K_BYTES + r0 * Gm::V_ROW), p.v + vo + r0 * Gm::V_ROW,
+                 vbytes, bar, policy);
+        if constexpr (VI8) {
+            const long long so = row_offset(p, b, kv, tok, Gm::S_ROW);
+            bulk_g2s(smem_u32(st + Gm::K_BYTES + Gm::V_BYTES), p.vs + so, Gm::S_BYTES, bar,
+                     policy);
+        }
+    };
+
+    if (lane == 0)
+        for (int j = 0; j < STAGES && j < n_my; ++j)
+            issue(j, j);
+    __syncwarp();
+
+    int j_fail = -1;
+    for (int j = 0; j < n_my; ++j) {
+        const int s = j % STAGES;
+        const uint32_t parity = (j / STAGES) & 1;
+        if (!mbar_wait_warp(my_bars + 8 * s, parity)) {
+            if (lane == 0)
+                flag(FA_STATUS_WAIT_TIMEOUT);
+            j_fail = j;
+            break;
+        }
+        const int ti = t_first + warp + j * NWARPS;
+        int r0, r1;
+        tile_rows(ti, r0, r1);
+        const bool block_ok = row_offset(p, b, kv, ti * TILE, 2) >= 0;
+        const unsigned char *st = my_stages + s * STAGE_BYTES;
+        const bool partial = (r0 != 0) || (r1 != TILE);
+
+        if (block_ok) {
+            // ---- QK: partial dots of this lane's chunks, GP heads x KH keys
+            float part[NV];
+#pragma unroll
+            for (int jj = 0; jj < KH; ++jj) {
+                const int t = 2 * jj + hw;
+                const __half *krow = reinterpret_cast<const __half *>(st) + t * D;
+                float kf[EPL];
+#pragma unroll
+                for (int c = 0; c < NCH; ++c)
+                    half8_to_float(*reinterpret_cast<const uint4 *>(krow + c * 128 + li * 8),
+                                   &kf[c * 8]);
+#pragma unroll
+                for (int g = 0; g < GP; ++g) {
+                    float sacc = 0.f;
+#pragma unroll
+                    for (int e = 0; e < EPL; ++e)
+                        sacc = fmaf(qf[g][e], kf[e], sacc);
+                    part[jj * GP + g] = sacc;
+                }
+            }
+            HalfWarpReduce<NV, 0>::run(part, li);
+#pragma unroll
+            for (int r = 0; r < NVL; ++r) {
+                const int idx = reduced_index<NV>(li, r);
+                const int t = 2 * (idx / GP) + hw;
+                float sv = part[r] * p.c2;
+                if (partial && (t < r0 || t >= r1))
+                    sv = -INFINITY;
+                sbuf[t * GP + idx % GP] = sv;
+            }
+            __syncwarp();
+
+            // ---- online softmax: tile max per head, rescale, weights
+            float sv[NR];
+            float tmax = -INFINITY;
+#pragma unroll
+            for (int r = 0; r < NR; ++r) {
+                const int i = lane + 32 * r;
+                sv[r] = (i < NSC) ? sbuf[i] : -INFINITY;
+                tmax = fmaxf(tmax, sv[r]);
+            }
+#pragma unroll
+            for (int mask = 16; mask >= GP; mask >>= 1)
+                tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, mask));
+            // lane holds the tile max of head (lane % GP); lane g holds head g
+            bool grow = false;
+            float mnew[GP];
+#pragma unroll
+            for (int g = 0; g < GP; ++g) {
+                mnew[g] = fmaxf(m_run[g], __shfl_sync(0xffffffffu, tmax, g));
+                grow |= mnew[g] > m_run[g];
+            }
+            const float mnew_mine = fmaxf(m_mine, tmax);
+            if (grow) {                              // identical in every lane
+#pragma unroll
+                for (int g = 0; g < GP; ++g) {
+                    const float a = ex2(m_run[g] - mnew[g]);
+#pragma unroll
+                    for (int e = 0; e < EPL; ++e)
+                        acc[g][e] *= a;
+                    m_run[g] = mnew[g];
+                }
+                l_lane *= ex2(m_mine - mnew_mine);
+                m_mine = mnew_mine;
+            }
+#pragma unroll
+            for (int r = 0; r < NR; ++r) {
+                const int i = lane + 32 * r;
+                if (i < NSC) {
+                    const float pv = ex2(sv[r] - m_mine);
+                    sbuf[i] = pv;
+                    l_lane += pv;
+                }
+            }
+            __syncwarp();
+
+            // ---- PV: acc[g][e] += p[t][g] * V[t][e] over this half-warp's keys
+#pragma unroll
+            for (int jj = 0; jj < KH; ++jj) {
+                const int t = 2 * jj + hw;
+                if (partial && (t < r0 || t >= r1))
+                    continue;
+                float pg[GP];
+#pragma unroll
+                for (int g = 0; g < GP; ++g)
+                    pg[g] = sbuf[t * GP + g];
+                if constexpr (!VI8) {
+                    const __half *vrow =
+                        reinterpret_cast<const __half *>(st + Gm::K_BYTES) + t * D;
+                    float vf[EPL];
+#pragma unroll
+                    for (int c = 0; c < NCH; ++c)
+                        half8_to_float(
+                            *reinterpret_cast<const uint4 *>(vrow + c * 128 + li * 8),
+                            &vf[c * 8]);
+#pragma unroll
+                    for (int g = 0; g < GP; ++g)
+#pragma unroll
+                        for (int e = 0; e < EPL; ++e)
+                            acc[g][e] = fmaf(pg[g], vf[e], acc[g][e]);
+                } else {
+                    const int8_t *vrow =
+                        reinterpret_cast<const int8_t *>(st + Gm::K_BYTES) + t * D;
+                    const __half *srow =
+                        reinterpret_cast<const __half *>(st + Gm::K_BYTES + Gm::V_BYTES) +
+                        t * (D / 32);
+#pragma unroll
+                    for (int c = 0; c < NCH; ++c) {
+                        const float sc = __half2float(srow[c * 4 + li / 4]);
+                        const uint2 raw =
+                            *reinterpret_cast<const uint2 *>(vrow + c * 128 + li * 8);
+                        const int8_t *cb = reinterpret_cast<const int8_t *>(&raw);
+#pragma unroll
+                        for (int g = 0; g < GP; ++g) {
+                            const float ps = pg[g] * sc;
+#pragma unroll
+                            for (int e = 0; e < 8; ++e)
+                                acc[g][c * 8 + e] =
+                                    fmaf(ps, static_cast<float>(cb[e]), acc[g][c * 8 + e]);
+                        }
+                    }
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0 && j + STAGES < n_my)
+            issue(j + STAGES, s);
+        __syncwarp();
+    }
+    if (j_fail >= 0) {
+        // Drain the copies still in flight into this warp's stages (each wait
+        // bounded again) so none lands after the CTA exits; this split's
+        // result is void and FA_STATUS_WAIT_TIMEOUT tells the host so.
+        for (int jj = j_fail; jj < n_my && jj < j_fail + STAGES; ++jj)
+            mbar_wait_warp(my_bars + 8 * (jj % STAGES), (jj / STAGES) & 1);
+    }
+
+    // ---- warp epilogue: complete sums, combine half-warps, publish to smem
+#pragma unroll
+    for (int mask = 16; mask >= GP; mask >>= 1)
+        l_lane += __shfl_xor_sync(0xffffffffu, l_lane, mask);
+#pragma unroll
+    for (int g = 0; g < GP; ++g)
+#pragma unroll
+        for (int e = 0; e < EPL; ++e)
+            acc[g][e] += __shfl_xor_sync(0xffffffffu, acc[g][e], 16);
+    if (hw == 0) {
+#pragma unroll
+        for (int g = 0; g < GP; ++g)
+#pragma unroll
+            for (int c = 0; c < NCH; ++c) {
+                float4 *dst = reinterpret_cast<float4 *>(ow + (warp * GP + g) * D + c * 128 +
+                                                         li * 8);
+                dst[0] = make_float4(acc[g][c * 8 + 0], acc[g][c * 8 + 1], acc[g][c * 8 + 2],
+                                     acc[g][c * 8 + 3]);
+                dst[1] = make_float4(acc[g][c * 8 + 4], acc[g][c * 8 + 5], acc[g][c * 8 + 6],
+                                     acc[g][c * 8 + 7]);
+            }
+    }
+    if (lane < GP) {
+        mw[warp * GP + lane] = m_mine;
+        lw[warp * GP + lane] = l_lane;
+    }
+    __syncthreads();
+
+    // ---- CTA merge of the NWARPS partial states (log-sum-exp), then write
+    const int nh = min(p.hpg, p.G - hg * p.hpg);
+    for (int idx = threadIdx.x; idx < nh * D; idx += THREADS) {
+        const int g = idx / D;
+        const int d = idx % D;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < NWARPS; ++w)
+            M = fmaxf(M, mw[w * GP + g]);
+        float L = 0.f, O = 0.f;
+        if (M != -INFINITY) {
+#pragma unroll
+            for (int w = 0; w < NWARPS; ++w) {
+                const float mwv = mw[w * GP + g];
+                const float a = (mwv == -INFINITY) ? 0.f : ex2(mwv - M);
+                L = fmaf(lw[w * GP + g], a, L);
+                O = fmaf(ow[(w * GP + g) * D + d], a, O);
+            }
+        }
+        const int h = kv * p.G + hg * p.hpg + g;
+        const long long row = (long long)b * p.Hq + h;
+        if (n_splits == 1) {
+            p.out[row * D + d] = L > 0.f ? O / L : 0.f;
+        } else {
+            p.ws_o[(row * p.max_splits + z) * D + d] = O;
+            if (d == 0)
+                p.ws_ml[row * p.max_splits + z] = make_float2(M, L);
+        }
+    }
+}
+
+// ---------------------------------------------------------------- merge kernel
+template <int D, int TILE>
+__global__ void __launch_bounds__(D / 4) fa_merge_kernel(const Params p)
+{
+    const long long row = blockIdx.x;
+    const int b = static_cast<int>(row / p.Hq);
+    int lo, hi;
+    attended_range(p, b, lo, hi, false);
+    const int nt = tiles_in<TILE>(lo, hi);
+    const int ns = (nt + p.tps - 1) / p.tps;
+    if (ns == 1)
+        return;                                   // the split kernel wrote this row
+    float4 *dst = reinterpret_cast<float4 *>(p.out + row * D) + threadIdx.x;
+    if (ns == 0) {
+        *dst = make_float4(0.f, 0.f, 0.f, 0.f);
+        return;
+    }
+    const float2 *ml = p.ws_ml + row * p.max_splits;
+    float M = -INFINITY;
+    for (int s = 0; s < ns; ++s)
+        M = fmaxf(M, ml[s].x);
+    float L = 0.f;
+    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s = 0; s < ns; ++s) {
+        const float2 v = ml[s];
+        const float a = (v.x == -INFINITY) ? 0.f : ex2(v.x - M);
+        L = fmaf(v.y, a, L);
+        const float4 x = reinterpret_cast<const float4 *>(p.ws_o + (row * p.max_splits + s) * D)
+            [threadIdx.x];
+        o.x = fmaf(x.x, a, o.x);
+        o.y = fmaf(x.y, a, o.y);
+        o.z = fmaf(x.z, a, o.z);
+        o.w = fmaf(x.w, a, o.w);
+    }
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    *dst = make_float4(o.x * inv, o.y * inv, o.z * inv, o.w * inv);
+}
+
+// ------------------------------------------------------------ int8 V packer
+// One warp per 32-element block: lane i quantises element i.
+__global__ void fa_quantize_kernel(const float *x, long long n_blocks, int8_t *codes,
+                                   __half *scales)
+{
+    const long long blk = (long long)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+    if (blk >= n_blocks)
+        return;
+    const int lane = threadIdx.x & 31;
+    const float xv = x[blk * 32 + lane];
+    float amax = fabsf(xv);
+#pragma unroll
+    for (int m = 16; m >= 1; m >>= 1)
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, m));
+    const __half sh = __double2half(static_cast<double>(amax) / 127.0);
+    const double s = static_cast<double>(__half2float(sh));
+    double qv = 0.0;
+    if (s != 0.0) {
+        qv = rint(static_cast<double>(xv) / s);
+        qv = fmin(fmax(qv, -127.0), 127.0);
+    }
+    codes[blk * 32 + lane] = static_cast<int8_t>(qv);
+    if (lane == 0)
+        scales[blk] = sh;
+}
+
+// ------------------------------------------------------------ gather (debug)
+__global__ void fa_gather_kernel(const Params p, int row_bytes, int b, int n_tokens,
+                                 unsigned char *dense)
+{
+    const int kv = blockIdx.y;
+    const int t = blockIdx.x;
+    if (t >= n_tokens)
+        return;
+    // same page-address path as the loader: tile start, then the row within it
+    const int tok = t - t % 16;
+    long long off = row_offset(p, b, kv, tok, row_bytes);
+    unsigned char *dst = dense + ((long long)kv * n_tokens + t) * row_bytes;
+    if (off < 0) {
+        if (threadIdx.x == 0)
+            flag(FA_STATUS_BAD_BLOCK);
+        for (int i = threadIdx.x; i < row_bytes; i += blockDim.x)
+            dst[i] = 0;
+        return;
+    }
+    off += (long long)(t - tok) * row_bytes;
+    const unsigned char *src = reinterpret_cast<const unsigned char *>(p.k) + off;
+    for (int i = threadIdx.x; i < row_bytes; i += blockDim.x)
+        dst[i] = src[i];
+}
+
+// ================================================================ host side
+static thread_local char g_err[512] = "";
+static thread_local cudaEvent_t g_prof_start = nullptr;
+static thread_local cudaEvent_t g_prof_end = nullptr;
+
+static int fail(int code, const char *fmt, ...) __attribute__((format(printf, 2, 3)));
+static int fail(int code, const char *fmt, ...)
+{
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof(g_err), fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+struct Plan {
+    int tile;
+    int gp;          // padded heads per CTA
+    int hpg;         // real heads per CTA
+    int n_hg;        // head groups per KV head
+    int tps;         // tiles per split
+    int max_splits;
+};
+
+static int next_pow2(int x)
+{
+    int p = 1;
+    while (p < x)
+        p <<= 1;
+    return p;
+}
+
+// Split planner: sizes splits from batch x kv_heads x capacity so that the
+// grid holds several waves of resident CTAs (the "nwg" of the pages, chosen
+// here from the SM count rather than a fixed bucket).
+static Plan make_plan(int B, int Hq, int Hkv, int D, long long cap, int num_sms)
+{
+    Plan pl;
+    pl.tile = 2048 / D;
+    const int G = Hq / Hkv;
+    const int gpmax = D == 128 ? 4 : 2;
+    if (G <= gpmax) {
+        pl.gp = next_pow2(G);
+        pl.hpg = G;
+        pl.n_hg = 1;
+    } else {
+        pl.gp = gpmax;
+        pl.hpg = gpmax;
+        pl.n_hg = (G + gpmax - 1) / gpmax;
+    }
+    const long long max_tiles = cap > 0 ? (cap + pl.tile - 1) / pl.tile : 1;
+    const long long units = (long long)B * Hkv * pl.n_hg;
+    const long long target = (long long)(num_sms > 0 ? num_sms : 1) * 2 /*CTAs/SM*/ * 4 /*waves*/;
+    long long tps = (units * max_tiles + target - 1) / target;
+    if (tps < NWARPS)
+        tps = NWARPS;
+    if (tps > 256)
+        tps = 256;
+    pl.tps = static_cast<int>(tps);
+    pl.max_splits = static_cast<int>((max_tiles + tps - 1) / tps);
+    return pl;
+}
+
+static size_t plan_workspace(const Plan &pl, int B, int Hq, int D)
+{
+    if (pl.max_splits <= 1)
+        return 0;
+    const size_t rows = (size_t)B * Hq * pl.max_splits;
+    const size_t o_bytes = rows * D * sizeof(float);
+    return o_bytes + rows * sizeof(float2);
+}
+
+static int device_sms(int *out)
+{
+    static std::mutex mu;
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return fail(FA_ERR_CUDA, "cudaGetDevice failed");
+    std::lock_guard<std::mutex> lock(mu);
+    if (dev < 64 && cache[dev] > 0) {
+        *out = cache[dev];
+        return 0;
+    }
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+        return fail(FA_ERR_CUDA, "cannot read the SM count of device %d", dev);
+    if (dev < 64)
+        cache[dev] = n;
+    *out = n;
+    return 0;
+}
+
+template <int D, int GP, bool VI8>
+static size_t split_smem()
+{
+    constexpr int NSC = Geo<D, VI8>::TILE * GP;
+    return (size_t)NWARPS * STAGES * STAGE_BYTES +
+           sizeof(float) * (NWARPS * NSC + 2 * NWARPS * GP + NWARPS * GP * D) +
+           sizeof(uint64_t) * NWARPS * STAGES;
+}
+
+template <int D, int GP, bool VI8>
+static cudaError_t launch_split(const Params &p, dim3 grid, cudaStream_t st)
+{
+    const size_t smem = split_smem<D, GP, VI8>();
+    static std::mutex mu;
+    static bool done[64] = {false};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (dev >= 64 || !done[dev]) {
+            e = cudaFuncSetAttribute(fa_split_kernel<D, GP, VI8>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            if (e != cudaSuccess)
+                return e;
+            if (dev < 64)
+                done[dev] = true;
+        }
+    }
+    fa_split_kernel<D, GP, VI8><<<grid, THREADS, smem, st>>>(p);
+    return cudaGetLastError();
+}
+
+template <int D, bool VI8>
+static cudaError_t dispatch_gp(const Params &p, int gp, dim3 grid, cudaStream_t st)
+{
+    switch (gp) {
+    case 1: return launch_split<D, 1, VI8>(p, grid, st);
+    case 2: return launch_split<D, 2, VI8>(p, grid, st);
+    default:
+        if constexpr (D == 128)
+            return launch_split<D, 4, VI8>(p, grid, st);
+        return cudaErrorInvalidValue;
+    }
+}
+
+static bool overlaps(const void *a, size_t na, const void *b, size_t nb)
+{
+    if (!a || !b || na == 0 || nb == 0)
+        return false;
+    const uintptr_t a0 = (uintptr_t)a, b0 = (uintptr_t)b;
+    return a0 < b0 + nb && b0 < a0 + na;
+}
+
+static bool aligned16(const void *x)
+{
+    return ((uintptr_t)x & 15u) == 0;
+}
+
+}  // namespace fa
+
+using namespace fa;
+
+extern "C" {
+
+FA_API const char *fa_decode_last_error(void)
+{
+    return g_err;
+}
+
+FA_API size_t fa_decode_workspace_size(int batch, int n_q_heads, int n_kv_heads, int head_dim,
+                                       int max_kv_len, int num_sms)
+{
+    if (batch < 0 || n_q_heads <= 0 || n_kv_heads <= 0 || n_q_heads % n_kv_heads ||
+        (head_dim != 128 && head_dim != 256) || max_kv_len < 0)
+        return 0;
+    if (num_sms <= 0 && device_sms(&num_sms) != 0)
+        return 0;
+    const Plan pl = make_plan(batch, n_q_heads, n_kv_heads, head_dim, max_kv_len, num_sms);
+    return plan_workspace(pl, batch, n_q_heads, head_dim);
+}
+
+FA_API int fa_decode(const void *q, const void *k_cache, const void *v_cache,
+                     const void *v_scales, const int32_t *block_table,
+                     const int32_t *seq_lens, int n_q_heads, int n_kv_heads, int head_dim,
+                     float scale, const int32_t *window, void *out, int batch, int page_size,
+                     int max_blocks_per_seq, int num_blocks, void *workspace,
+                     size_t workspace_bytes, void *stream)
+{
+    g_err[0] = 0;
+    if (!q || !k_cache || !v_cache || !seq_lens || !out)
+        return fail(FA_ERR_NULL, "fa_decode: q, k_cache, v_cache, seq_lens and out are required");
+    if (head_dim != 128 && head_dim != 256)
+        return fail(FA_ERR_HEAD_DIM, "fa_decode: head_dim %d not supported (128 or 256)", head_dim);
+    if (n_q_heads <= 0 || n_kv_heads <= 0 || n_q_heads % n_kv_heads ||
+        n_q_heads / n_kv_heads > 64)
+        return fail(FA_ERR_HEADS, "fa_decode: bad heads (q %d, kv %d)", n_q_heads, n_kv_heads);
+    if (!isfinite(scale))
+        return fail(FA_ERR_SCALE, "fa_decode: scale is not finite");
+    if (batch < 0 || batch > 65535 || max_blocks_per_seq <= 0 || n_kv_heads > 4096)
+        return fail(FA_ERR_LAYOUT, "fa_decode: bad batch %d, max_blocks_per_seq %d or kv heads %d",
+                    batch, max_blocks_per_seq, n_kv_heads);
+    const bool paged = block_table != nullptr;
+    const bool vi8 = v_scales != nullptr;
+    long long cap;
+    if (paged) {
+        if (page_size <= 0 || page_size % 16)
+            return fail(FA_ERR_LAYOUT, "fa_decode: page_size %d must be a positive multiple of 16",
+                        page_size);
+        if (num_blocks <= 0)
+            return fail(FA_ERR_LAYOUT, "fa_decode: num_blocks must be positive when paged");
+        cap = (long long)max_blocks_per_seq * page_size;
+    } else {
+        cap = max_blocks_per_seq;
+        if (vi8 && cap % 16)
+            return fail(FA_ERR_LAYOUT,
+                        "fa_decode: contiguous int8-V capacity %lld must be a multiple of 16", cap);
+    }
+    if (cap > (1ll << 30))
+        return fail(FA_ERR_LAYOUT, "fa_decode: capacity %lld tokens too large", cap);
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
+        (vi8 && !aligned16(v_scales)) || (workspace && !aligned16(workspace)))
+        return fail(FA_ERR_ALIGN, "fa_decode: q, k_cache, v_cache, v_scales, out and workspace "
+                                  "must be 16-byte aligned");
+    const int D = head_dim;
+    // aliasing: out against every input range we can size
+    const size_t out_bytes = (size_t)batch * n_q_heads * D * sizeof(float);
+    const size_t rows = paged ? (size_t)num_blocks * page_size : (size_t)batch * cap;
+    const size_t kv_rows = rows * n_kv_heads;
+    if (overlaps(out, out_bytes, q, (size_t)batch * n_q_heads * D * 2) ||
+        overlaps(out, out_bytes, k_cache, kv_rows * D * 2) ||
+        overlaps(out, out_bytes, v_cache, kv_rows * D * (vi8 ? 1 : 2)) ||
+        (vi8 && overlaps(out, out_bytes, v_scales, kv_rows * (D / 32) * 2)) ||
+        overlaps(out, out_bytes, seq_lens, (size_t)batch * 4) ||
+        (paged && overlaps(out, out_bytes, block_table, (size_t)batch * max_blocks_per_seq * 4)) ||
+        (window && overlaps(out, out_bytes, window, (size_t)batch * 4)))
+        return fail(FA_ERR_ALIAS, "fa_decode: out overlaps an input or the workspace");
+    int sms = 0;
+    int rc = device_sms(&sms);
+    if (rc)
+        return rc;
+    const Plan pl = make_plan(batch, n_q_heads, n_kv_heads, D, cap, sms);
+    const size_t need = plan_workspace(pl, batch, n_q_heads, D);
+    if (need > 0 && (!workspace || workspace_bytes < need))
+        return fail(FA_ERR_WORKSPACE, "fa_decode: workspace %zu bytes, need %zu", workspace_bytes,
+                    need);
+    if (overlaps(out, out_bytes, workspace, need))
+        return fail(FA_ERR_ALIAS, "fa_decode: out overlaps the workspace");
+    if (batch == 0)
+        return 0;
+
+    Params p;
+    p.q = static_cast<const __half *>(q);
+    p.k = static_cast<const char *>(k_cache);
+    p.v = static_cast<const char *>(v_cache);
+    p.vs = static_cast<const char *>(v_scales);
+    p.bt = block_table;
+    p.seq_lens = seq_lens;
+    p.window = window;
+    p.out = static_cast<float *>(out);
+    p.ws_o = static_cast<float *>(workspace);
+    p.ws_ml = need ? reinterpret_cast<float2 *>(static_cast<char *>(workspace) +
+                                                (size_t)batch * n_q_heads * pl.max_splits * D *
+                                                    sizeof(float))
+                   : nullptr;
+    p.B = batch;
+    p.Hq = n_q_heads;
+    p.Hkv = n_kv_heads;
+    p.G = n_q_heads / n_kv_heads;
+    p.n_hg = pl.n_hg;
+    p.hpg = pl.hpg;
+    p.page_size = paged ? page_size : 16;
+    p.max_blocks = max_blocks_per_seq;
+    p.num_blocks = num_blocks;
+    p.cap = cap;
+    p.c2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+    p.tps = pl.tps;
+    p.max_splits = pl.max_splits;
+
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const dim3 grid(pl.max_splits, n_kv_heads * pl.n_hg, batch);
+    cudaEvent_t prof_start = g_prof_start, prof_end = g_prof_end;
+    g_prof_start = g_prof_end = nullptr;
+    cudaError_t e = cudaSuccess;
+    if (prof_start)
+        e = cudaEventRecord(prof_start, st);
+    if (e != cudaSuccess)
+        return fail(FA_ERR_CUDA, "fa_decode: profile event: %s", cudaGetErrorString(e));
+    if (D == 128)
+        e = vi8 ? dispatch_gp<128, true>(p, pl.gp, grid, st)
+                : dispatch_gp<128, false>(p, pl.gp, grid, st);
+    else
+        e = vi8 ? dispatch_gp<256, true>(p, pl.gp, grid, st)
+                : dispatch_gp<256, false>(p, pl.gp, grid, st);
+    if (e != cudaSuccess)
+        return fail(FA_ERR_CUDA, "fa_decode: split launch failed: %s", cudaGetErrorString(e));
+    if (prof_end && (e = cudaEventRecord(prof_end, st)) != cudaSuccess)
+        return fail(FA_ERR_CUDA, "fa_decode: profile event: %s", cudaGetErrorString(e));
+    if (D == 128)
+        fa_merge_kernel<128, 16><<<batch * n_q_heads, 32, 0, st>>>(p);
+    else
+        fa_merge_kernel<256, 8><<<batch * n_q_heads, 64, 0, st>>>(p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess)
+        return fail(FA_ERR_CUDA, "fa_decode: merge launch failed: %s", cudaGetErrorString(e));
+    return 0;
+}
+
+FA_API int fa_quantize_v_int8(const float *x, long long n_rows, int head_dim, int8_t *codes,
+                              void *scales, void *stream)
+{
+    g_err[0] = 0;
+    if (!x || !codes || !scales)
+        return fail(FA_ERR_NULL, "fa_quantize_v_int8: null pointer");
+    if (head_dim <= 0 || head_dim % 32 || n_rows < 0)
+        return fail(FA_ERR_HEAD_DIM, "fa_quantize_v_int8: head_dim %d must be a positive "
+                                     "multiple of 32", head_dim);
+    const long long n_blocks = n_rows * (head_dim / 32);
+    if (n_blocks == 0)
+        return 0;
+    const int per_cta = 8;   // warps per CTA
+    const long long ctas = (n_blocks + per_cta - 1) / per_cta;
+    if (ctas > 0x7fffffffll)
+        return fail(FA_ERR_LAYOUT, "fa_quantize_v_int8: too many rows");
+    fa_quantize_kernel<<<(unsigned)ctas, per_cta * 32, 0, static_cast<cudaStream_t>(stream)>>>(
+        x, n_blocks, codes, static_cast<__half *>(scales));
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess)
+        return fail(FA_ERR_CUDA, "fa_quantize_v_int8: launch failed: %s", cudaGetErrorString(e));
+    return 0;
+}
+
+FA_API int fa_gather_kv_debug(const void *cache, int row_bytes, const int32_t *block_table,
+                              int b, int n_kv_heads, int page_size, int max_blocks_per_seq,
+                              int num_blocks, int n_tokens, void *dense, void *stream)
+{
+    g_err[0] = 0;
+    if (!cache || !dense)
+        return fail(FA_ERR_NULL, "fa_gather_kv_debug: null pointer");
+    const bool paged = block_table != nullptr;
+    if (row_bytes <= 0 || n_kv_heads <= 0 || b < 0 || n_tokens < 0 || max_blocks_per_seq <= 0 ||
+        (paged && (page_size <= 0 || page_size % 16 || num_blocks <= 0)))
+        return fail(FA_ERR_LAYOUT, "fa_gather_kv_debug: bad sizes");
+    const long long cap = paged ? (long long)max_blocks_per_seq * page_size : max_blocks_per_seq;
+    if (n_tokens > cap)
+        return fail(FA_ERR_LAYOUT, "fa_gather_kv_debug: n_tokens %d > capacity %lld", n_tokens,
+                    cap);
+    if (n_tokens == 0)
+        return 0;
+    Params p;
+    memset(&p, 0, sizeof(p));
+    p.k = static_cast<const char *>(cache);
+    p.bt = block_table;
+    p.Hkv = n_kv_heads;
+    p.page_size = paged ? page_size : 16;
+    p.max_blocks = max_blocks_per_seq;
+    p.num_blocks = num_blocks;
+    p.cap = cap;
+    fa_gather_kernel<<<dim3(n_tokens, n_kv_heads), 128, 0, static_cast<cudaStream_t>(stream)>>>(
+        p, row_bytes, b, n_tokens, static_cast<unsigned char *>(dense));
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess)
+        return fail(FA_ERR_CUDA, "fa_gather_kv_debug: launch failed: %s", cudaGetErrorString(e));
+    return 0;
+}
+
+FA_API int fa_decode_profile_next(void *split_start, void *split_end)
+{
+    g_err[0] = 0;
+    g_prof_start = static_cast<cudaEvent_t>(split_start);
+    g_prof_end = static_cast<cudaEvent_t>(split_end);
+    return 0;
+}
+
+FA_API int fa_decode_device_status(unsigned int *status, void *stream)
+{
+    g_err[0] = 0;
+    if (!status)
+        return fail(FA_ERR_NULL, "fa_decode_device_status: null pointer");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    unsigned int v = 0;
+    const unsigned int zero = 0;
+    cudaError_t e = cudaMemcpyFromSymbolAsync(&v, g_status, sizeof(v), 0,
+                                              cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess)
+        e = cudaMemcpyToSymbolAsync(g_status, &zero, sizeof(zero), 0, cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess)
+        e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess)
+        return fail(FA_ERR_CUDA, "fa_decode_device_status: %s", cudaGetErrorString(e));
+    *status = v;
+    return 0;
+}
+
+}  // extern "C"

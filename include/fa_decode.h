@@ -1,0 +1,166 @@
+/*
+ * fa_decode.h -- C ABI of the GB300 (sm_103a) decode-step attention library.
+ *
+ * One call computes, for every sequence b and query head h of a decode step,
+ *
+ *     out[b][h][:] = softmax(scale * q[b][h] . K_b[kv][t] for t in [lo_b, L_b)) @ V_b[kv]
+ *
+ * with kv = h / (n_q_heads / n_kv_heads), L_b = seq_lens[b] and
+ * lo_b = (window[b] > 0 && L_b > window[b]) ? L_b - window[b] : 0.
+ * Sources (mlx-native page "flash_attn_vec_hybrid.metal", kernel
+ * flash_attn_vec_hybrid_impl and its batched / GQA siblings):
+ *   - GQA head map: the "map query head to KV head" step;
+ *   - length and sliding-window rule: the per-chunk mask block (keys with
+ *     logical index < kv_seq_len - sliding_window are masked, window 0 =
+ *     global, the tessl page "nn.rs" flash_attn_decode: "window == 0 selects
+ *     the global rule");
+ *   - online softmax over KV blocks and the split-K partial (O, S, M) with a
+ *     log-sum-exp merge: the "Online softmax" block, the cross-simdgroup
+ *     reduce and the NWG > 1 partial write, and the separate reduce pass
+ *     (flash_attn_vec_reduce, tessl flash_attn_decode_reduce);
+ *   - an empty attended range gives a zero row ("S == 0 ? 0").
+ * The int8 V variant stores V as int8 codes times one fp16 scale per 32
+ * consecutive head_dim elements (dequantisation as ggml block_q8_0 on the
+ * DS4Server page "dsv4_hc.metal").
+ *
+ * All pointers passed to fa_decode are DEVICE pointers unless stated, owned
+ * by the caller; the library allocates nothing, keeps no pointer after
+ * return, and enqueues all work on `stream` (a cudaStream_t; NULL = legacy
+ * default stream) without synchronising.  Every function returns 0 on success
+ * or a negative FA_ERR_* code; nothing is launched when a check fails, and
+ * fa_decode_last_error() returns a message for the calling thread's last
+ * failure.
+ */
+#ifndef FA_DECODE_H
+#define FA_DECODE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define FA_API __attribute__((visibility("default")))
+
+/* Error codes. */
+#define FA_OK 0
+#define FA_ERR_NULL (-1)        /* a required pointer is NULL */
+#define FA_ERR_HEAD_DIM (-2)    /* head_dim not 128 or 256 */
+#define FA_ERR_HEADS (-3)       /* heads <= 0, or n_q_heads % n_kv_heads != 0, or group > 64 */
+#define FA_ERR_WORKSPACE (-4)   /* workspace smaller than fa_decode_workspace_size() */
+#define FA_ERR_SCALE (-5)       /* scale not finite */
+#define FA_ERR_LAYOUT (-6)      /* bad batch / page_size / block counts / capacity */
+#define FA_ERR_ALIAS (-7)       /* out overlaps an input or the workspace */
+#define FA_ERR_CUDA (-8)        /* a CUDA call or kernel launch failed */
+#define FA_ERR_ALIGN (-9)       /* a tensor is not 16-byte aligned */
+
+/* Device-side status bits, reported by fa_decode_device_status(). */
+#define FA_STATUS_LEN_CLAMPED 1u   /* a seq_lens entry was < 0 or > capacity and was clamped */
+#define FA_STATUS_BAD_BLOCK 2u     /* a block-table entry was outside [0, num_blocks); tile skipped */
+#define FA_STATUS_WAIT_TIMEOUT 4u  /* a copy wait passed its ~1 s limit; that split's result is void */
+
+/*
+ * fa_decode -- one decode step of attention for `batch` sequences.
+ *
+ * q          [batch][n_q_heads][head_dim] fp16.
+ * k_cache    fp16 keys.  Paged (block_table != NULL):
+ *              [num_blocks][n_kv_heads][page_size][head_dim];
+ *            contiguous (block_table == NULL):
+ *              [batch][n_kv_heads][capacity][head_dim], capacity = max_blocks_per_seq.
+ * v_cache    values, same layout as k_cache: fp16 when v_scales == NULL, else int8.
+ * v_scales   NULL (fp16 V) or the fp16 scales of int8 V, one per 32 head_dim
+ *            elements: [...same leading dims as v_cache...][head_dim / 32].
+ * block_table int32 [batch][max_blocks_per_seq]: logical page p of sequence b
+ *            lives in physical block block_table[b][p]; only the pages that
+ *            hold keys in the attended range are read.  NULL = contiguous.
+ * seq_lens   int32 [batch]: keys in each sequence's cache (the current token
+ *            included).  Values outside [0, capacity] are clamped on the
+ *            device and flagged (FA_STATUS_LEN_CLAMPED).
+ * window     int32 [batch] sliding-window sizes (0 = global), or NULL (all global).
+ * scale      softmax scale applied to q.k (e.g. 1/sqrt(head_dim)).
+ * out        [batch][n_q_heads][head_dim] fp32, written in full (zero rows
+ *            for empty ranges).  Must not overlap any input or the workspace.
+ * batch      number of sequences (0 is a no-op).
+ * page_size  tokens per physical block, a positive multiple of 16 (ignored
+ *            when contiguous).
+ * max_blocks_per_seq  block-table row length (paged), or the per-sequence
+ *            capacity in tokens (contiguous; a multiple of 16 for int8 V).
+ * num_blocks physical blocks in the paged caches (bounds for block ids;
+ *            ignored when contiguous).
+ * workspace  device scratch of at least fa_decode_workspace_size() bytes,
+ *            16-byte aligned; contents need no initialisation and are not
+ *            preserved.  May be NULL when that size is 0.
+ * stream     cudaStream_t to enqueue on.
+ *
+ * q, k_cache, v_cache, v_scales and out must be 16-byte aligned.
+ */
+FA_API int fa_decode(const void *q, const void *k_cache, const void *v_cache,
+                     const void *v_scales, const int32_t *block_table,
+                     const int32_t *seq_lens, int n_q_heads, int n_kv_heads, int head_dim,
+                     float scale, const int32_t *window, void *out, int batch, int page_size,
+                     int max_blocks_per_seq, int num_blocks, void *workspace,
+                     size_t workspace_bytes, void *stream);
+
+/*
+ * fa_decode_workspace_size -- bytes of scratch fa_decode needs for these
+ * sizes: the split-K partials (unnormalised O plus running max and sum per
+ * query head and split; the "partial scratch B*H*chunks*(D+2)" of tessl's
+ * flash_attn_decode).  max_kv_len is the per-sequence capacity in tokens
+ * (max_blocks_per_seq * page_size when paged).  num_sms <= 0 queries the
+ * current device; pass the same value fa_decode will see (it uses the
+ * current device's SM count).  Host-only; never launches.  Returns 0 for
+ * invalid sizes.
+ */
+FA_API size_t fa_decode_workspace_size(int batch, int n_q_heads, int n_kv_heads, int head_dim,
+                                       int max_kv_len, int num_sms);
+
+/*
+ * fa_quantize_v_int8 -- pack fp32 values into the int8 V cache format.
+ * x [n_rows][head_dim] fp32 (device) -> codes [n_rows][head_dim] int8 and
+ * scales [n_rows][head_dim/32] fp16 (device).  Per block of 32 elements:
+ * s = fp16 round-to-nearest-even(max|x| / 127); code = clamp(round-half-even(
+ * x / s), -127, 127), all zero when s == 0.  (The pages print only the
+ * dequantisation, ggml block_q8_0 on the DS4Server page "dsv4_hc.metal";
+ * this quantiser is the plain symmetric reading.)  head_dim % 32 == 0.
+ */
+FA_API int fa_quantize_v_int8(const float *x, long long n_rows, int head_dim, int8_t *codes,
+                              void *scales, void *stream);
+
+/*
+ * fa_gather_kv_debug -- copy sequence b's first n_tokens cache rows, through
+ * the same page-address path fa_decode's loader uses, into dense
+ * [n_kv_heads][n_tokens][row_bytes] (device).  row_bytes = 2*head_dim for K
+ * or fp16 V, head_dim for int8 V, head_dim/16 for the scales.  A byte copy;
+ * exists so the block-table indirection can be checked bit for bit.
+ * Block ids are range-checked against num_blocks (FA_ERR_LAYOUT on the host
+ * is impossible for device tables; bad ids leave zero rows and set
+ * FA_STATUS_BAD_BLOCK).
+ */
+FA_API int fa_gather_kv_debug(const void *cache, int row_bytes, const int32_t *block_table,
+                              int b, int n_kv_heads, int page_size, int max_blocks_per_seq,
+                              int num_blocks, int n_tokens, void *dense, void *stream);
+
+/*
+ * fa_decode_device_status -- wait for `stream`, then read and clear the
+ * device-side FA_STATUS_* bits accumulated since the last call.
+ */
+FA_API int fa_decode_device_status(unsigned int *status, void *stream);
+
+/*
+ * fa_decode_profile_next -- instrumentation for timing.  The next fa_decode
+ * call made on this host thread records the cudaEvent_t `split_start` on its
+ * stream just before its split-K kernel and `split_end` just after it (the
+ * merge kernel follows), then forgets both.  Either may be NULL.  No work is
+ * skipped or changed.
+ */
+FA_API int fa_decode_profile_next(void *split_start, void *split_end);
+
+/* Message for the calling thread's last failed call ("" if none). */
+FA_API const char *fa_decode_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_DECODE_H */

@@ -1,0 +1,106 @@
+"""Host-side checks of the C-ABI library (no GPU needed).
+
+The library loads, exports every entry point include/fa_decode.h declares,
+and rejects bad arguments with the documented codes before touching the GPU.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+from decode_step_kv_gb300 import _build, binding
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_symbols():
+    names = []
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            names += re.findall(r"FA_API\s+[\w\s\*]+?\b(\w+)\s*\(", text)
+    return names
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return binding.load()
+
+
+def test_header_declares_the_boundary():
+    names = declared_symbols()
+    for required in ("fa_decode", "fa_decode_workspace_size"):
+        assert required in names
+    assert len(names) == len(set(names))
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+        assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
+
+
+def test_library_built_for_sm_103a_only():
+    text = open(_build.__file__).read()
+    assert "arch=compute_103a,code=sm_103a" in text
+    assert "sm_90" not in text and "sm_100" not in text
+
+
+# ------------------------------------------------------------------ validation
+A = 1 << 20  # fake, 16-byte aligned "device" addresses: never dereferenced
+
+
+def call(lib, **kw):
+    args = dict(q=A, k=2 * A, v=3 * A, vs=None, bt=None, sl=4 * A, hq=8, hkv=2, d=128,
+                scale=0.088, win=None, out=5 * A, batch=1, page=16, maxb=512, nblk=0,
+                ws=6 * A, wsb=1 << 30, stream=None)
+    args.update(kw)
+    rc = lib.fa_decode(args["q"], args["k"], args["v"], args["vs"], args["bt"], args["sl"],
+                       args["hq"], args["hkv"], args["d"], args["scale"], args["win"],
+                       args["out"], args["batch"], args["page"], args["maxb"], args["nblk"],
+                       args["ws"], args["wsb"], args["stream"])
+    return rc, lib.fa_decode_last_error().decode()
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), -1), (dict(k=None), -1), (dict(v=None), -1), (dict(sl=None), -1),
+    (dict(out=None), -1),
+    (dict(d=64), -2), (dict(d=192), -2),
+    (dict(hq=6, hkv=4), -3), (dict(hkv=0), -3), (dict(hq=0), -3), (dict(hq=130, hkv=2), -3),
+    (dict(scale=float("inf")), -5), (dict(scale=float("nan")), -5),
+    (dict(batch=-1), -6), (dict(maxb=0), -6),
+    (dict(bt=7 * A, page=8, nblk=10), -6), (dict(bt=7 * A, page=24, nblk=10), -6),
+    (dict(bt=7 * A, page=16, nblk=0), -6),
+    (dict(vs=8 * A, maxb=500), -6),                      # contiguous int8 needs cap % 16 == 0
+    (dict(q=A + 8), -9), (dict(out=5 * A + 4), -9), (dict(k=2 * A + 2), -9),
+    (dict(out=2 * A + 64), -7),                          # out inside the K cache
+    (dict(out=A), -7),                                   # out == q
+])
+def test_bad_arguments_rejected_before_any_launch(lib, kw, code):
+    rc, msg = call(lib, **kw)
+    assert rc == code, msg
+    assert msg
+
+
+def test_workspace_size_host_only(lib):
+    f = lib.fa_decode_workspace_size
+    assert f(1, 8, 2, 100, 512, 152) == 0                  # bad head_dim
+    assert f(1, 6, 4, 128, 512, 152) == 0                  # heads not divisible
+    small = f(1, 8, 2, 128, 512, 152)
+    big = f(32, 32, 8, 128, 32768, 152)
+    # partial O (D floats) plus (m, l) per query head and split
+    assert small % (8 * (128 * 4 + 8)) == 0
+    assert big % (32 * 32 * (128 * 4 + 8)) == 0
+    assert big > small > 0
+    # more SMs -> at least as many splits
+    assert f(32, 32, 8, 128, 32768, 304) >= big
+    assert f(0, 8, 2, 128, 512, 152) == 0
+
+
+def test_quantize_and_gather_reject_bad_arguments(lib):
+    assert lib.fa_quantize_v_int8(None, 1, 32, A, A, None) == -1
+    assert lib.fa_quantize_v_int8(A, 1, 48, A, A, None) == -2
+    assert lib.fa_gather_kv_debug(A, 256, None, 0, 2, 16, 64, 0, 65, A, None) == -6
+    assert lib.fa_gather_kv_debug(A, 256, A, 0, 2, 8, 64, 4, 16, A, None) == -6
+    assert lib.fa_gather_kv_debug(None, 256, None, 0, 2, 16, 64, 0, 16, A, None) == -1
