@@ -20,8 +20,8 @@ sample of the same workload (the reference arm of this benchmark).
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
-import math
 import os
 import statistics
 import subprocess
@@ -48,6 +48,8 @@ def parse_args():
     ap.add_argument("--only", action="store_true", help="measure only --workload (for profiling)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="profiling only: keep the first N sequences of --workload")
     return ap.parse_args()
 
 
@@ -211,6 +213,7 @@ def time_kernel(wl, d, steps, warmup, world, device, clocks_gpu=None):
         if flush is not None:
             flush.fill_(i & 0xFF)
         ev[i][0].record(stream)
+        ev[i][1].record(stream)   # creates the event; the library re-records it after the split kernel
         binding.fa_decode_profile_next(None, ev[i][1])
         call(wl, d, stream)
         ev[i][2].record(stream)
@@ -286,7 +289,7 @@ def oracle_sample(wl, inp, budget_s, threads=0):
     n_units = wl.batch * wl.n_kv_heads
     per_call = max(1, -(-n_threads // G))       # enough rows to keep every core busy
     done_bytes, elapsed, units, start, used = 0, 0.0, 0, 0, 1
-    while elapsed < budget_s and units < 4 * n_units:
+    while elapsed < budget_s:
         chunk = [(start + i) % n_units for i in range(per_call)]
         start += per_call
         rows = []
@@ -333,6 +336,9 @@ def run_ours(args, world, rank, local):
     binding.load()
     peak, peak_kind = measured_peaks()
     wl = WORKLOADS[args.workload]
+    if args.batch:
+        wl = dataclasses.replace(wl, batch=args.batch, seq_lens=None if wl.seq_lens is None
+                                 else wl.seq_lens[:args.batch])
     d = prepare(wl, device)
     gpu_index = int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[0]) \
         if os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")[0].isdigit() else local

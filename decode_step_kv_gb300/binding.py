@@ -126,9 +126,15 @@ def fa_gather_kv_debug(cache, row_bytes, block_table, b, n_kv_heads, page_size,
 
 
 def fa_decode_profile_next(split_start=None, split_end=None):
-    """Record torch.cuda.Event objects around the next call's split kernel."""
+    """Record torch.cuda.Event objects around the next call's split kernel.
+
+    The events must already exist on the device (torch creates them lazily at
+    their first record()); a zero handle raises.
+    """
     a = None if split_start is None else ctypes.c_void_p(split_start.cuda_event)
     b = None if split_end is None else ctypes.c_void_p(split_end.cuda_event)
+    if (split_start is not None and not a.value) or (split_end is not None and not b.value):
+        raise ValueError("fa_decode_profile_next: event not created yet (record it once first)")
     _check(load().fa_decode_profile_next(a, b))
 
 

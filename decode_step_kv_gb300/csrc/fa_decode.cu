@@ -24,8 +24,10 @@
 // passes deriving the same live split count from the device-side length so
 // the scratch needs no zero fill.  Scores are kept in the base-2 domain
 // (scale * log2 e folded into one multiplier), which changes no result.
+#include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 #include <math.h>
 #include <stdarg.h>
 #include <stdint.h>
@@ -33,6 +35,7 @@
 #include <string.h>
 
 #include <mutex>
+#include <stdlib.h>
 
 #include "../../include/fa_decode.h"
 
@@ -77,6 +80,7 @@ struct Params {
     int page_size, max_blocks, num_blocks;
     long long cap;    // tokens per sequence
     float c2;         // scale * log2(e)
+    int tile;         // tokens per tile
     int tps;          // tiles per split
     int max_splits;
 };
@@ -582,15 +586,367 @@ __global__ void __launch_bounds__(THREADS, 2) fa_split_kernel(const Params p)
     }
 }
 
+// ------------------------------------------------------ tensor-core split kernel
+// Same split / merge contract as fa_split_kernel, with the two contractions on
+// the tensor cores.  Per 16-key tile and per warp:
+//   S[16 keys x 8 heads]   = K_tile[16 x D] . Q^T[D x 8]       (D/16 mma.m16n8k16)
+//   O^T[D x 8 heads]      += V_tile^T[D x 16] . P^T[16 x 8]     (D/16 mma.m16n8k16)
+// The query heads of one KV head sit on the N = 8 dimension (a group of up to
+// 8 heads is one dense column block; larger groups split into head groups).
+// K and V tiles arrive by TMA tiled copies (cp.async.bulk.tensor, 64-column
+// boxes, 128-byte swizzle), so the ldmatrix row reads are bank-conflict-free.
+// P is rounded to fp16 for the PV product (accumulation stays fp32); its
+// C-fragment is transposed into the B operand with movmatrix.
+namespace tc {
+
+constexpr int TILE = 16;
+constexpr int NWARPS = 4;
+constexpr int GPH = 8;          // heads per CTA (the mma N dimension)
+
+template <int D>
+struct Cfg {
+    static constexpr int STAGES = D == 128 ? 3 : 2;
+    static constexpr int BOXES = D / 64;                  // 64-column boxes per row
+    static constexpr int BOX_BYTES = TILE * 128;          // 16 rows x 128 B
+    static constexpr int T_BYTES = BOXES * BOX_BYTES;     // one tensor's tile (K or V)
+    static constexpr int STAGE_BYTES = 2 * T_BYTES;
+    static constexpr int RING_BYTES = NWARPS * STAGES * STAGE_BYTES;
+    static constexpr int MERGE_BYTES = sizeof(float) * (NWARPS * GPH * D + 2 * NWARPS * GPH);
+    static constexpr int SMEM = (RING_BYTES > MERGE_BYTES ? RING_BYTES : MERGE_BYTES) +
+                                NWARPS * STAGES * 8 + 1024;   // + barriers + alignment slack
+};
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y,
+                                            uint32_t bar, uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
+                                        uint32_t &r3)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &r0, uint32_t &r1,
+                                          uint32_t &r2, uint32_t &r3)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1)
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, "
+        "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x)
+{
+    uint32_t y;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
+}
+
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi)
+{
+    const __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t *>(&h);
+}
+
+// Shared address of 16-byte chunk `chunk` (0..D/8-1) of tile row `row` in a
+// tile of BOXES swizzled 64-column boxes.
+__device__ __forceinline__ uint32_t swz(uint32_t base, int row, int chunk)
+{
+    const int box = chunk >> 3;
+    const int c = (chunk & 7) ^ (row & 7);
+    return base + box * (TILE * 128) + row * 128 + c * 16;
+}
+
+// Tile row coordinate (the tensor maps view K and V as [rows][D]); -1 for a
+// block id out of range.
+__device__ __forceinline__ long long tile_row(const Params &p, int b, int kv, int tok)
+{
+    if (p.bt) {
+        const long long blk = p.bt[(long long)b * p.max_blocks + tok / p.page_size];
+        if (blk < 0 || blk >= p.num_blocks)
+            return -1;
+        return (blk * p.Hkv + kv) * p.page_size + tok % p.page_size;
+    }
+    return ((long long)b * p.Hkv + kv) * p.cap + tok;
+}
+
+template <int D>
+__global__ void __launch_bounds__(NWARPS * 32, 1)
+    fa_split_mma_kernel(const Params p, const __grid_constant__ CUtensorMap tmK,
+                        const __grid_constant__ CUtensorMap tmV)
+{
+    using C = Cfg<D>;
+    constexpr int STAGES = C::STAGES;
+    constexpr int KS = D / 16;                       // k-steps of QK, m-tiles of PV
+
+    const int z = blockIdx.x;
+    const int kv = blockIdx.y / p.n_hg;
+    const int hg = blockIdx.y % p.n_hg;
+    const int b = blockIdx.z;
+
+    int lo, hi;
+    attended_range(p, b, lo, hi, z == 0 && blockIdx.y == 0 && threadIdx.x == 0);
+    const int nt = tiles_in<TILE>(lo, hi);
+    const int n_splits = (nt + p.tps - 1) / p.tps;
+    if (z >= n_splits)
+        return;
+    const int t_first = lo / TILE + z * p.tps;
+    const int t_count = min(p.tps, nt - z * p.tps);
+
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char *smem = reinterpret_cast<unsigned char *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(
+        smem + (C::RING_BYTES > C::MERGE_BYTES ? C::RING_BYTES : C::MERGE_BYTES));
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int g4 = lane >> 2;        // fragment row group
+    const int t4 = lane & 3;         // fragment column pair
+    const uint32_t ring = smem_u32(smem) + warp * STAGES * C::STAGE_BYTES;
+    const uint32_t my_bars = smem_u32(bars + warp * STAGES);
+
+    if (lane == 0)
+        for (int s = 0; s < STAGES; ++s)
+            mbar_init(my_bars + 8 * s, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    __syncwarp();
+
+    const int nh = min(GPH, p.G - hg * GPH);         // real heads in this CTA
+    // Q^T as the QK B operand: b0 = q[head g4][16ks + 2t4 .. +1], b1 = +8
+    uint32_t qb[KS][2];
+    {
+        const bool live = g4 < nh;
+        const __half *qrow = p.q + ((long long)b * p.Hq + kv * p.G + hg * GPH + g4) * D;
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+            qb[ks][0] = live ? *reinterpret_cast<const uint32_t *>(qrow + ks * 16 + 2 * t4) : 0u;
+            qb[ks][1] = live ? *reinterpret_cast<const uint32_t *>(qrow + ks * 16 + 8 + 2 * t4)
+                             : 0u;
+        }
+    }
+
+    float acc[KS][4];
+#pragma unroll
+    for (int i = 0; i < KS; ++i)
+        acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+    float m0 = -INFINITY, m1 = -INFINITY;    // running max, heads 2t4 and 2t4+1
+    float l0 = 0.f, l1 = 0.f;                // this lane's share of the sums
+
+    const uint64_t policy = evict_first_policy();
+    const int n_my = t_count > warp ? (t_count - warp + NWARPS - 1) / NWARPS : 0;
+
+    auto issue = [&](int j, int s) {
+        const int ti = t_first + warp + j * NWARPS;
+        const uint32_t bar = my_bars + 8 * s;
+        const long long row = tile_row(p, b, kv, ti * TILE);
+        if (row < 0) {
+            flag(FA_STATUS_BAD_BLOCK);
+            mbar_expect_tx(bar, 0);
+            return;
+        }
+        mbar_expect_tx(bar, C::STAGE_BYTES);
+        const uint32_t st = ring + s * C::STAGE_BYTES;
+#pragma unroll
+        for (int bx = 0; bx < C::BOXES; ++bx) {
+            tma_load_2d(st + bx * C::BOX_BYTES, &tmK, bx * 64, (int)row, bar, policy);
+            tma_load_2d(st + C::T_BYTES + bx * C::BOX_BYTES, &tmV, bx * 64, (int)row, bar,
+                        policy);
+        }
+    };
+
+    if (lane == 0)
+        for (int j = 0; j < STAGES && j < n_my; ++j)
+            issue(j, j);
+    __syncwarp();
+
+    int j_fail = -1;
+    for (int j = 0; j < n_my; ++j) {
+        const int s = j % STAGES;
+        if (!mbar_wait_warp(my_bars + 8 * s, (j / STAGES) & 1)) {
+            if (lane == 0)
+                flag(FA_STATUS_WAIT_TIMEOUT);
+            j_fail = j;
+            break;
+        }
+        const int ti = t_first + warp + j * NWARPS;
+        const int base = ti * TILE;
+        const int r0 = max(lo - base, 0);
+        const int r1 = min(hi - base, TILE);
+        const bool block_ok = tile_row(p, b, kv, base) >= 0;
+        const uint32_t sK = ring + s * C::STAGE_BYTES;
+        const uint32_t sV = sK + C::T_BYTES;
+
+        if (block_ok) {
+            if (r0 != 0 || r1 != TILE) {
+                // keys outside [r0, r1) hold other tokens' data: zero their V
+                // rows (a 128-byte row segment per box) so 0-weights stay 0
+                for (int i = lane; i < TILE * C::BOXES * 8; i += 32) {
+                    const int row = i / (C::BOXES * 8);
+                    if (row < r0 || row >= r1) {
+                        const int rem = i % (C::BOXES * 8);
+                        const uint32_t a = sV + (rem >> 3) * C::BOX_BYTES + row * 128 +
+                                           (rem & 7) * 16;
+                        asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(a), "r"(0)
+                                     : "memory");
+                    }
+                }
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                __syncwarp();
+            }
+            // ---- S = K . Q^T  (rows: keys g4, g4+8; cols: heads 2t4, 2t4+1)
+            float sc[4] = {0.f, 0.f, 0.f, 0.f};
+            {
+                const int mi = lane >> 3;
+                const int krow = (mi & 1) * 8 + (lane & 7);
+#pragma unroll
+                for (int ks = 0; ks < KS; ++ks) {
+                    uint32_t a0, a1, a2, a3;
+                    ldsm_x4(swz(sK, krow, ks * 2 + (mi >> 1)), a0, a1, a2, a3);
+                    mma16816(sc, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
+                }
+            }
+            const bool va = g4 >= r0 && g4 < r1;
+            const bool vb = g4 + 8 >= r0 && g4 + 8 < r1;
+            sc[0] = va ? sc[0] * p.c2 : -INFINITY;
+            sc[1] = va ? sc[1] * p.c2 : -INFINITY;
+            sc[2] = vb ? sc[2] * p.c2 : -INFINITY;
+            sc[3] = vb ? sc[3] * p.c2 : -INFINITY;
+            // ---- online softmax per head (lanes sharing t4 share the heads)
+            float x0 = fmaxf(sc[0], sc[2]);
+            float x1 = fmaxf(sc[1], sc[3]);
+#pragma unroll
+            for (int mask = 4; mask <= 16; mask <<= 1) {
+                x0 = fmaxf(x0, __shfl_xor_sync(0xffffffffu, x0, mask));
+                x1 = fmaxf(x1, __shfl_xor_sync(0xffffffffu, x1, mask));
+            }
+            const float n0 = fmaxf(m0, x0);
+            const float n1 = fmaxf(m1, x1);
+            if (__any_sync(0xffffffffu, n0 > m0 || n1 > m1)) {
+                const float a0 = ex2(m0 - n0);
+                const float a1 = ex2(m1 - n1);
+#pragma unroll
+                for (int i = 0; i < KS; ++i) {
+                    acc[i][0] *= a0;
+                    acc[i][1] *= a1;
+                    acc[i][2] *= a0;
+                    acc[i][3] *= a1;
+                }
+                l0 *= a0;
+                l1 *= a1;
+                m0 = n0;
+                m1 = n1;
+            }
+            const float p0 = ex2(sc[0] - m0), p1 = ex2(sc[1] - m1);
+            const float p2 = ex2(sc[2] - m0), p3 = ex2(sc[3] - m1);
+            l0 += p0 + p2;
+            l1 += p1 + p3;
+            // ---- P^T as the PV B operand (keys x heads), via movmatrix
+            const uint32_t pb0 = movmatrix_t(pack_half2(p0, p1));
+            const uint32_t pb1 = movmatrix_t(pack_half2(p2, p3));
+            // ---- O^T += V^T . P^T  (rows: head_dim; cols: heads)
+            {
+                const int mi = lane >> 3;
+                const int vrow = (mi >> 1) * 8 + (lane & 7);
+#pragma unroll
+                for (int mt = 0; mt < KS; ++mt) {
+                    uint32_t a0, a1, a2, a3;
+                    ldsm_x4_t(swz(sV, vrow, mt * 2 + (mi & 1)), a0, a1, a2, a3);
+                    mma16816(acc[mt], a0, a1, a2, a3, pb0, pb1);
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0 && j + STAGES < n_my)
+            issue(j + STAGES, s);
+        __syncwarp();
+    }
+    if (j_fail >= 0)
+        for (int jj = j_fail; jj < n_my && jj < j_fail + STAGES; ++jj)
+            mbar_wait_warp(my_bars + 8 * (jj % STAGES), (jj / STAGES) & 1);
+
+    // ---- warp epilogue: complete the sums, publish (O, m, l) per head
+#pragma unroll
+    for (int mask = 4; mask <= 16; mask <<= 1) {
+        l0 += __shfl_xor_sync(0xffffffffu, l0, mask);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, mask);
+    }
+    __syncthreads();                                  // every warp done with the ring
+    float *ow = reinterpret_cast<float *>(smem);      // [NWARPS][GPH][D]
+    float *mw = ow + NWARPS * GPH * D;                // [NWARPS][GPH]
+    float *lw = mw + NWARPS * GPH;
+#pragma unroll
+    for (int mt = 0; mt < KS; ++mt) {
+        float *o = ow + (warp * GPH + 2 * t4) * D + mt * 16 + g4;
+        o[0] = acc[mt][0];
+        o[D] = acc[mt][1];
+        o[8] = acc[mt][2];
+        o[D + 8] = acc[mt][3];
+    }
+    if (g4 == 0) {
+        mw[warp * GPH + 2 * t4] = m0;
+        mw[warp * GPH + 2 * t4 + 1] = m1;
+        lw[warp * GPH + 2 * t4] = l0;
+        lw[warp * GPH + 2 * t4 + 1] = l1;
+    }
+    __syncthreads();
+
+    for (int idx = threadIdx.x; idx < nh * D; idx += NWARPS * 32) {
+        const int g = idx / D;
+        const int d = idx % D;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < NWARPS; ++w)
+            M = fmaxf(M, mw[w * GPH + g]);
+        float L = 0.f, O = 0.f;
+        if (M != -INFINITY) {
+#pragma unroll
+            for (int w = 0; w < NWARPS; ++w) {
+                const float mwv = mw[w * GPH + g];
+                const float a = (mwv == -INFINITY) ? 0.f : ex2(mwv - M);
+                L = fmaf(lw[w * GPH + g], a, L);
+                O = fmaf(ow[(w * GPH + g) * D + d], a, O);
+            }
+        }
+        const long long row = (long long)b * p.Hq + kv * p.G + hg * GPH + g;
+        if (n_splits == 1) {
+            p.out[row * D + d] = L > 0.f ? O / L : 0.f;
+        } else {
+            p.ws_o[(row * p.max_splits + z) * D + d] = O;
+            if (d == 0)
+                p.ws_ml[row * p.max_splits + z] = make_float2(M, L);
+        }
+    }
+}
+
+}  // namespace tc
+
 // ---------------------------------------------------------------- merge kernel
-template <int D, int TILE>
+template <int D>
 __global__ void __launch_bounds__(D / 4) fa_merge_kernel(const Params p)
 {
     const long long row = blockIdx.x;
     const int b = static_cast<int>(row / p.Hq);
     int lo, hi;
     attended_range(p, b, lo, hi, false);
-    const int nt = tiles_in<TILE>(lo, hi);
+    const int nt = hi > lo ? (hi - 1) / p.tile - lo / p.tile + 1 : 0;
     const int ns = (nt + p.tps - 1) / p.tps;
     if (ns == 1)
         return;                                   // the split kernel wrote this row
@@ -686,8 +1042,11 @@ static int fail(int code, const char *fmt, ...)
     return code;
 }
 
+enum class Path { Simt, Mma };
+
 struct Plan {
-    int tile;
+    Path path;
+    int tile;        // tokens per tile
     int gp;          // padded heads per CTA
     int hpg;         // real heads per CTA
     int n_hg;        // head groups per KV head
@@ -703,27 +1062,49 @@ static int next_pow2(int x)
     return p;
 }
 
+// Which split kernel serves a call: the tensor-core kernel for fp16 V, the
+// CUDA-core kernel for int8 V.  FA_DECODE_KERNEL=simt|mma overrides (for A/B
+// measurements); both compute the same result within the tolerances.
+static Path choose_path(bool vi8)
+{
+    const char *e = getenv("FA_DECODE_KERNEL");
+    if (vi8 || (e && !strcmp(e, "simt")))
+        return Path::Simt;
+    return Path::Mma;
+}
+
 // Split planner: sizes splits from batch x kv_heads x capacity so that the
 // grid holds several waves of resident CTAs (the "nwg" of the pages, chosen
 // here from the SM count rather than a fixed bucket).
-static Plan make_plan(int B, int Hq, int Hkv, int D, long long cap, int num_sms)
+static Plan make_plan(Path path, int B, int Hq, int Hkv, int D, long long cap, int num_sms)
 {
     Plan pl;
-    pl.tile = 2048 / D;
+    pl.path = path;
     const int G = Hq / Hkv;
-    const int gpmax = D == 128 ? 4 : 2;
-    if (G <= gpmax) {
-        pl.gp = next_pow2(G);
-        pl.hpg = G;
-        pl.n_hg = 1;
+    int ctas_per_sm;
+    if (path == Path::Mma) {
+        pl.tile = tc::TILE;
+        pl.gp = tc::GPH;
+        pl.hpg = tc::GPH;
+        pl.n_hg = (G + tc::GPH - 1) / tc::GPH;
+        ctas_per_sm = D == 128 ? 2 : 1;
     } else {
-        pl.gp = gpmax;
-        pl.hpg = gpmax;
-        pl.n_hg = (G + gpmax - 1) / gpmax;
+        pl.tile = 2048 / D;
+        const int gpmax = D == 128 ? 4 : 2;
+        if (G <= gpmax) {
+            pl.gp = next_pow2(G);
+            pl.hpg = G;
+            pl.n_hg = 1;
+        } else {
+            pl.gp = gpmax;
+            pl.hpg = gpmax;
+            pl.n_hg = (G + gpmax - 1) / gpmax;
+        }
+        ctas_per_sm = 2;
     }
     const long long max_tiles = cap > 0 ? (cap + pl.tile - 1) / pl.tile : 1;
     const long long units = (long long)B * Hkv * pl.n_hg;
-    const long long target = (long long)(num_sms > 0 ? num_sms : 1) * 2 /*CTAs/SM*/ * 4 /*waves*/;
+    const long long target = (long long)(num_sms > 0 ? num_sms : 1) * ctas_per_sm * 4 /*waves*/;
     long long tps = (units * max_tiles + target - 1) / target;
     if (tps < NWARPS)
         tps = NWARPS;
@@ -811,6 +1192,67 @@ static cudaError_t dispatch_gp(const Params &p, int gp, dim3 grid, cudaStream_t 
     }
 }
 
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no -lcuda).
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000,
+                                             cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            f = nullptr;
+        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    }();
+    return fn;
+}
+
+// A K or V cache viewed as a 2-D fp16 tensor [rows][D], loaded in boxes of
+// 16 rows x 64 columns with the 128-byte swizzle.
+static int encode_kv_map(CUtensorMap *map, const void *base, long long rows, int D)
+{
+    auto enc = tensor_map_encoder();
+    if (!enc)
+        return fail(FA_ERR_CUDA, "fa_decode: cuTensorMapEncodeTiled unavailable");
+    const cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)D * 2};
+    const cuuint32_t box[2] = {64, (cuuint32_t)tc::TILE};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(base), dims,
+                           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(FA_ERR_CUDA, "fa_decode: cuTensorMapEncodeTiled failed (%d)", (int)r);
+    return 0;
+}
+
+template <int D>
+static cudaError_t launch_mma(const Params &p, const CUtensorMap &tmK, const CUtensorMap &tmV,
+                              dim3 grid, cudaStream_t st)
+{
+    const int smem = tc::Cfg<D>::SMEM;
+    static std::mutex mu;
+    static bool done[64] = {false};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (dev >= 64 || !done[dev]) {
+            e = cudaFuncSetAttribute(tc::fa_split_mma_kernel<D>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+            if (e != cudaSuccess)
+                return e;
+            if (dev < 64)
+                done[dev] = true;
+        }
+    }
+    tc::fa_split_mma_kernel<D><<<grid, tc::NWARPS * 32, smem, st>>>(p, tmK, tmV);
+    return cudaGetLastError();
+}
+
 static bool overlaps(const void *a, size_t na, const void *b, size_t nb)
 {
     if (!a || !b || na == 0 || nb == 0)
@@ -843,8 +1285,15 @@ FA_API size_t fa_decode_workspace_size(int batch, int n_q_heads, int n_kv_heads,
         return 0;
     if (num_sms <= 0 && device_sms(&num_sms) != 0)
         return 0;
-    const Plan pl = make_plan(batch, n_q_heads, n_kv_heads, head_dim, max_kv_len, num_sms);
-    return plan_workspace(pl, batch, n_q_heads, head_dim);
+    // the caller's V type is not known here: size for whichever kernel needs more
+    size_t need = 0;
+    for (Path path : {Path::Simt, Path::Mma}) {
+        const Plan pl = make_plan(path, batch, n_q_heads, n_kv_heads, head_dim, max_kv_len,
+                                  num_sms);
+        const size_t n = plan_workspace(pl, batch, n_q_heads, head_dim);
+        need = n > need ? n : need;
+    }
+    return need;
 }
 
 FA_API int fa_decode(const void *q, const void *k_cache, const void *v_cache,
@@ -906,7 +1355,12 @@ FA_API int fa_decode(const void *q, const void *k_cache, const void *v_cache,
     int rc = device_sms(&sms);
     if (rc)
         return rc;
-    const Plan pl = make_plan(batch, n_q_heads, n_kv_heads, D, cap, sms);
+    Path path = choose_path(vi8);
+    const long long kv_rows_total = paged ? (long long)num_blocks * n_kv_heads * page_size
+                                          : (long long)batch * n_kv_heads * cap;
+    if (kv_rows_total >= (1ll << 31))
+        path = Path::Simt;   // TMA row coordinates are 32-bit
+    const Plan pl = make_plan(path, batch, n_q_heads, n_kv_heads, D, cap, sms);
     const size_t need = plan_workspace(pl, batch, n_q_heads, D);
     if (need > 0 && (!workspace || workspace_bytes < need))
         return fail(FA_ERR_WORKSPACE, "fa_decode: workspace %zu bytes, need %zu", workspace_bytes,
@@ -941,6 +1395,7 @@ FA_API int fa_decode(const void *q, const void *k_cache, const void *v_cache,
     p.num_blocks = num_blocks;
     p.cap = cap;
     p.c2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+    p.tile = pl.tile;
     p.tps = pl.tps;
     p.max_splits = pl.max_splits;
 
@@ -953,20 +1408,29 @@ FA_API int fa_decode(const void *q, const void *k_cache, const void *v_cache,
         e = cudaEventRecord(prof_start, st);
     if (e != cudaSuccess)
         return fail(FA_ERR_CUDA, "fa_decode: profile event: %s", cudaGetErrorString(e));
-    if (D == 128)
-        e = vi8 ? dispatch_gp<128, true>(p, pl.gp, grid, st)
-                : dispatch_gp<128, false>(p, pl.gp, grid, st);
-    else
-        e = vi8 ? dispatch_gp<256, true>(p, pl.gp, grid, st)
-                : dispatch_gp<256, false>(p, pl.gp, grid, st);
+    if (e == cudaSuccess && pl.path == Path::Mma) {
+        CUtensorMap tmK, tmV;
+        const int rk = encode_kv_map(&tmK, k_cache, kv_rows_total, D);
+        const int rv = rk ? rk : encode_kv_map(&tmV, v_cache, kv_rows_total, D);
+        if (rk || rv)
+            return rk ? rk : rv;
+        e = D == 128 ? launch_mma<128>(p, tmK, tmV, grid, st) : launch_mma<256>(p, tmK, tmV, grid, st);
+    } else if (e == cudaSuccess) {
+        if (D == 128)
+            e = vi8 ? dispatch_gp<128, true>(p, pl.gp, grid, st)
+                    : dispatch_gp<128, false>(p, pl.gp, grid, st);
+        else
+            e = vi8 ? dispatch_gp<256, true>(p, pl.gp, grid, st)
+                    : dispatch_gp<256, false>(p, pl.gp, grid, st);
+    }
     if (e != cudaSuccess)
         return fail(FA_ERR_CUDA, "fa_decode: split launch failed: %s", cudaGetErrorString(e));
     if (prof_end && (e = cudaEventRecord(prof_end, st)) != cudaSuccess)
         return fail(FA_ERR_CUDA, "fa_decode: profile event: %s", cudaGetErrorString(e));
     if (D == 128)
-        fa_merge_kernel<128, 16><<<batch * n_q_heads, 32, 0, st>>>(p);
+        fa_merge_kernel<128><<<batch * n_q_heads, 32, 0, st>>>(p);
     else
-        fa_merge_kernel<256, 8><<<batch * n_q_heads, 64, 0, st>>>(p);
+        fa_merge_kernel<256><<<batch * n_q_heads, 64, 0, st>>>(p);
     e = cudaGetLastError();
     if (e != cudaSuccess)
         return fail(FA_ERR_CUDA, "fa_decode: merge launch failed: %s", cudaGetErrorString(e));

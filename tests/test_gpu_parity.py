@@ -48,8 +48,15 @@ SMALL = [
 ]
 
 
+@pytest.fixture(params=["mma", "simt"])
+def kernel(request, monkeypatch):
+    """Run a case through each split kernel (int8 V always takes the CUDA-core one)."""
+    monkeypatch.setenv("FA_DECODE_KERNEL", request.param)
+    return request.param
+
+
 @pytest.mark.parametrize("wl,lens", SMALL, ids=[w.name for w, _ in SMALL])
-def test_small_cases_match_oracle(wl, lens):
+def test_small_cases_match_oracle(wl, lens, kernel):
     cap = max(lens)
     if wl.v_int8 and not wl.paged:
         cap = -(-cap // 16) * 16
@@ -62,7 +69,7 @@ def test_small_cases_match_oracle(wl, lens):
             assert np.all(got[b] == 0)
 
 
-def test_run_to_run_bit_identical():
+def test_run_to_run_bit_identical(kernel):
     wl = W("det", 4, 8, 2, 128, paged=True)
     inp = to_cuda(build_case(wl, seq_lens=[100, 2000, 3000, 17], spare_blocks=2))
     a = gpu_decode(wl, inp).cpu()
@@ -70,7 +77,7 @@ def test_run_to_run_bit_identical():
     assert torch.equal(a, b)
 
 
-def test_batched_equals_one_sequence_at_a_time():
+def test_batched_equals_one_sequence_at_a_time(kernel):
     """A multi-sequence call equals single-sequence calls (within tolerance;
     the split plans differ, so bitwise equality is not required)."""
     wl = W("batched", 4, 8, 2, 128, paged=True)
@@ -100,7 +107,7 @@ def test_non_default_stream():
     assert_close(got.cpu().numpy(), want, False, "stream")
 
 
-def test_length_beyond_capacity_is_clamped_and_flagged():
+def test_length_beyond_capacity_is_clamped_and_flagged(kernel):
     wl = W("clamp", 2, 8, 2, 128, paged=True)
     inp = build_case(wl, seq_lens=[64, 32])
     binding.fa_decode_device_status()                       # clear
@@ -117,7 +124,7 @@ def test_length_beyond_capacity_is_clamped_and_flagged():
     assert_close(got[1], want[1], False, "clamped seq 1 (only its 32 stored keys)")
 
 
-def test_bad_block_id_is_skipped_and_flagged():
+def test_bad_block_id_is_skipped_and_flagged(kernel):
     wl = W("badblk", 2, 8, 2, 128, paged=True)
     inp = build_case(wl, seq_lens=[64, 64])
     dinp = to_cuda(inp)
@@ -213,7 +220,7 @@ def _oracle_rows_paged(wl, dinp, rows, v_codes=None, v_scales=None):
 
 
 @pytest.mark.parametrize("name", ["cfg1", "cfg2"])
-def test_small_workloads_full_oracle(name):
+def test_small_workloads_full_oracle(name, kernel):
     wl = WORKLOADS[name]
     inp = build_case(wl)
     want = oracle_decode(wl, inp)
