@@ -41,6 +41,9 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
             lib.fa_decode.argtypes = [P, P, P, P, P, P, i32, i32, i32, f32, P, P, i32, i32, i32,
                                       i32, P, sz, P]
             lib.fa_decode.restype = i32
+            lib.fa_decode_noalloc.argtypes = [P, P, P, P, P, P, i32, i32, i32, f32, P, P, i32,
+                                              i32, i32, i32, P]
+            lib.fa_decode_noalloc.restype = i32
             lib.fa_decode_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32]
             lib.fa_decode_workspace_size.restype = sz
             lib.fa_quantize_v_int8.argtypes = [P, i64, i32, P, P, P]
@@ -106,6 +109,29 @@ def fa_decode(q, k_cache, v_cache, v_scales, block_table, seq_lens, n_q_heads, n
                           int(head_dim), float(scale), _ptr(window), _ptr(out), int(batch),
                           int(page_size), int(max_blocks_per_seq), int(num_blocks),
                           _ptr(workspace), ws_bytes, _stream(stream))
+    _check(rc)
+
+
+def fa_decode_noalloc(q, k_cache, v_cache, v_scales, block_table, seq_lens, n_q_heads,
+                      n_kv_heads, head_dim, scale, window, out, *, batch=None, page_size=16,
+                      max_blocks_per_seq=None, num_blocks=None, stream=None):
+    """fa_decode without a workspace argument, for callers that cannot allocate.
+
+    The scratch is a fixed array inside the library (FA_NOALLOC_SCRATCH_BYTES);
+    sizes that need more raise FaDecodeError.  Calls that overlap on the GPU
+    share that array and race, so keep them on one stream.
+    """
+    if batch is None:
+        batch = q.shape[0]
+    if max_blocks_per_seq is None:
+        max_blocks_per_seq = block_table.shape[1] if block_table is not None else k_cache.shape[2]
+    if num_blocks is None:
+        num_blocks = k_cache.shape[0] if block_table is not None else 0
+    rc = load().fa_decode_noalloc(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(v_scales),
+                                  _ptr(block_table), _ptr(seq_lens), int(n_q_heads),
+                                  int(n_kv_heads), int(head_dim), float(scale), _ptr(window),
+                                  _ptr(out), int(batch), int(page_size),
+                                  int(max_blocks_per_seq), int(num_blocks), _stream(stream))
     _check(rc)
 
 

@@ -1266,6 +1266,36 @@ static bool aligned16(const void *x)
     return ((uintptr_t)x & 15u) == 0;
 }
 
+// Scratch for fa_decode_noalloc: a fixed array in the module image, so that
+// entry point needs no allocation.  Host code must not use the symbol's
+// host-side name as a device address; noalloc_scratch() returns the real one.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[FA_NOALLOC_SCRATCH_BYTES];
+
+// Device address of g_noalloc_scratch on the current device, looked up once
+// per device (with that device current) and cached.
+static int noalloc_scratch(void **out)
+{
+    static std::mutex mu;
+    static void *cache[64] = {nullptr};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return fail(FA_ERR_CUDA, "fa_decode_noalloc: cudaGetDevice failed");
+    std::lock_guard<std::mutex> lock(mu);
+    if (dev < 64 && cache[dev]) {
+        *out = cache[dev];
+        return 0;
+    }
+    void *ptr = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+    if (e != cudaSuccess || !ptr)
+        return fail(FA_ERR_CUDA, "fa_decode_noalloc: cannot find the scratch array on device %d: %s",
+                    dev, cudaGetErrorString(e));
+    if (dev < 64)
+        cache[dev] = ptr;
+    *out = ptr;
+    return 0;
+}
+
 }  // namespace fa
 
 using namespace fa;
@@ -1493,6 +1523,42 @@ FA_API int fa_gather_kv_debug(const void *cache, int row_bytes, const int32_t *b
     if (e != cudaSuccess)
         return fail(FA_ERR_CUDA, "fa_gather_kv_debug: launch failed: %s", cudaGetErrorString(e));
     return 0;
+}
+
+FA_API int fa_decode_noalloc(const void *q, const void *k_cache, const void *v_cache,
+                             const void *v_scales, const int32_t *block_table,
+                             const int32_t *seq_lens, int n_q_heads, int n_kv_heads,
+                             int head_dim, float scale, const int32_t *window, void *out,
+                             int batch, int page_size, int max_blocks_per_seq, int num_blocks,
+                             void *stream)
+{
+    g_err[0] = 0;
+    if (head_dim != 128 && head_dim != 256)
+        return fail(FA_ERR_HEAD_DIM, "fa_decode_noalloc: head_dim %d not supported (128 or 256)",
+                    head_dim);
+    if (n_q_heads <= 0 || n_kv_heads <= 0 || n_q_heads % n_kv_heads)
+        return fail(FA_ERR_HEADS, "fa_decode_noalloc: bad heads (q %d, kv %d)", n_q_heads,
+                    n_kv_heads);
+    if (batch < 0 || max_blocks_per_seq <= 0 || (block_table && page_size <= 0))
+        return fail(FA_ERR_LAYOUT, "fa_decode_noalloc: bad batch, capacity or page size");
+    const long long cap = block_table ? (long long)max_blocks_per_seq * page_size
+                                      : (long long)max_blocks_per_seq;
+    if (cap > (1ll << 30))
+        return fail(FA_ERR_LAYOUT, "fa_decode_noalloc: capacity %lld tokens too large", cap);
+    const size_t need = fa_decode_workspace_size(batch, n_q_heads, n_kv_heads, head_dim,
+                                                 (int)cap, 0);
+    if (need > FA_NOALLOC_SCRATCH_BYTES)
+        return fail(FA_ERR_WORKSPACE,
+                    "fa_decode_noalloc: these sizes need %zu bytes of scratch, more than the "
+                    "library's fixed %u bytes; use fa_decode with a caller workspace",
+                    need, (unsigned)FA_NOALLOC_SCRATCH_BYTES);
+    void *scratch = nullptr;
+    const int rc = noalloc_scratch(&scratch);
+    if (rc)
+        return rc;
+    return fa_decode(q, k_cache, v_cache, v_scales, block_table, seq_lens, n_q_heads,
+                     n_kv_heads, head_dim, scale, window, out, batch, page_size,
+                     max_blocks_per_seq, num_blocks, scratch, FA_NOALLOC_SCRATCH_BYTES, stream);
 }
 
 FA_API int fa_decode_profile_next(void *split_start, void *split_end)

@@ -148,6 +148,44 @@ FA_API int fa_gather_kv_debug(const void *cache, int row_bytes, const int32_t *b
 FA_API int fa_decode_device_status(unsigned int *status, void *stream);
 
 /*
+ * fa_decode_noalloc -- fa_decode for callers that cannot allocate device
+ * memory.  The pages have no counterpart; this is a deployment convenience.
+ *
+ * Some callers cannot call cudaMalloc (or any allocator) at the point where
+ * they run attention: for example a plugin inside a host framework that owns
+ * every device allocation through its own pool and forbids side allocations,
+ * or code on a latency-critical path where an allocation's implicit device
+ * synchronisation is not acceptable.  Such a caller still owns and passes
+ * every input and the output, but has no workspace to give.
+ *
+ * This entry point takes the same arguments as fa_decode minus the
+ * workspace, and runs the same kernels with their split-K scratch placed in a
+ * fixed array compiled into the library (FA_NOALLOC_SCRATCH_BYTES, 8 MiB).
+ * Every GPU that loads the library holds that array until the process exits.
+ * It allocates nothing and calls no allocating routine.
+ *
+ * Limits and rules:
+ *   - sizes whose scratch need (fa_decode_workspace_size) exceeds
+ *     FA_NOALLOC_SCRATCH_BYTES are rejected with FA_ERR_WORKSPACE and a
+ *     message stating both sizes; nothing is launched;
+ *   - the first call on a device looks up the array's device address on that
+ *     device (once per device, with it current); make that first call before
+ *     any stream capture begins;
+ *   - all calls share the one array: calls whose kernels overlap on the GPU
+ *     (different streams, or different host threads on one device) race on
+ *     it and give wrong results.  Serialise them, e.g. on one stream.  The
+ *     scratch needs no clearing between calls (every value read in a call is
+ *     written earlier in that call).
+ */
+#define FA_NOALLOC_SCRATCH_BYTES (8u << 20)
+FA_API int fa_decode_noalloc(const void *q, const void *k_cache, const void *v_cache,
+                             const void *v_scales, const int32_t *block_table,
+                             const int32_t *seq_lens, int n_q_heads, int n_kv_heads,
+                             int head_dim, float scale, const int32_t *window, void *out,
+                             int batch, int page_size, int max_blocks_per_seq, int num_blocks,
+                             void *stream);
+
+/*
  * fa_decode_profile_next -- instrumentation for timing.  The next fa_decode
  * call made on this host thread records the cudaEvent_t `split_start` on its
  * stream just before its split-K kernel and `split_end` just after it (the

@@ -1,0 +1,64 @@
+"""The allocation-free entry point (fa_decode_noalloc) against fa_decode.
+
+fa_decode_noalloc serves callers that cannot allocate device memory: it runs
+the same kernels with their split-K scratch in a fixed array inside the
+library.  This file is collected last so a run that stops at the first
+failure has already run every other test; it also passes on its own.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+from decode_step_kv_gb300 import binding
+from decode_step_kv_gb300.inputs import Workload
+
+from _helpers import assert_close, build_case, gpu_decode, to_cuda
+
+pytestmark = pytest.mark.gpu
+
+# scratch limit compiled into the library (include/fa_decode.h)
+NOALLOC_BYTES = 8 << 20
+
+
+def _noalloc(wl, d):
+    out = torch.full((wl.batch, wl.n_q_heads, wl.head_dim), float("nan"), dtype=torch.float32,
+                     device="cuda")
+    binding.fa_decode_noalloc(d["q"], d["k_cache"], d["v_cache"], d.get("v_scales"),
+                              d["block_table"], d["seq_lens"], wl.n_q_heads, wl.n_kv_heads,
+                              wl.head_dim, wl.scale, d["window"], out, batch=wl.batch,
+                              page_size=wl.page_size, max_blocks_per_seq=d["max_blocks"],
+                              num_blocks=d["num_blocks"] if wl.paged else 0)
+    return out
+
+
+@pytest.mark.parametrize("v_int8", [False, True])
+def test_noalloc_matches_fa_decode_on_two_calls_in_a_row(v_int8):
+    wl = Workload("noalloc", 4, 16, 4, 128, paged=True, v_int8=v_int8, window=1000,
+                  window_odd_only=True, seed=4242)
+    # the first call uses long sequences (many splits), the second short and
+    # ragged ones, so the second reads only scratch it wrote itself
+    for lens in ([9000, 12000, 7000, 16000], [300, 17, 5000, 1]):
+        inp = build_case(wl, seq_lens=lens, capacity=16000)
+        d = to_cuda(inp)
+        cap = d["max_blocks"] * wl.page_size
+        assert binding.fa_decode_workspace_size(4, 16, 4, 128, cap) > 0   # scratch is used
+        want = gpu_decode(wl, d).cpu().numpy()
+        got = _noalloc(wl, d)
+        torch.cuda.synchronize()
+        got = got.cpu().numpy()
+        assert_close(got, want, v_int8, f"noalloc lens={lens}")
+
+
+def test_noalloc_rejects_sizes_beyond_its_scratch():
+    B, Hq, Hkv, D, cap = 256, 64, 8, 256, 1 << 20
+    need = binding.fa_decode_workspace_size(B, Hq, Hkv, D, cap)
+    assert need > NOALLOC_BYTES
+    lib = binding.load()
+    A = 1 << 20   # never dereferenced: the call must fail before any launch
+    rc = lib.fa_decode_noalloc(A, 2 * A, 3 * A, None, None, 4 * A, Hq, Hkv, D, 0.06, None,
+                               5 * A, B, 16, cap, 0, None)
+    assert rc == -4
+    msg = lib.fa_decode_last_error().decode()
+    assert str(need) in msg and str(NOALLOC_BYTES) in msg
