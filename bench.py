@@ -10,8 +10,9 @@ listed under "configs".
 Timing: W untimed warm-up steps, then K timed steps bracketed by a barrier and
 torch.cuda.synchronize() on both sides; each step is timed with CUDA events on
 the launching stream.  When a workload's KV bytes are under 4x the L2 size,
-L2 is flushed (a 512 MiB buffer is written) before every timed step, outside
-its events.  The split kernel's own duration comes from events the library
+the steps cycle through enough copies of the inputs that every step reads
+inputs evicted from L2 (more than 4x L2 of other data read since their last
+use); larger workloads read more than L2 per step anyway.  The split kernel's own duration comes from events the library
 records around it (fa_decode_profile_next) on the same stream.
 
 --impl reference times the fp64 CPU oracle on the host cores on a bounded
@@ -187,22 +188,44 @@ def call(wl, d, stream, out=None):
                       stream=stream)
 
 
+INPUT_KEYS = ("q", "k_cache", "v_cache", "v_scales", "block_table", "seq_lens", "window")
+
+
+def rotation(d, nbytes):
+    """Copies of the step's inputs to cycle through so that each timed step
+    reads inputs that are not in L2: enough copies that the bytes read between
+    two uses of one copy exceed 4x the L2 size.  A single copy when the step's
+    own KV bytes already do."""
+    if nbytes >= 4 * L2_BYTES:
+        return [d], "inputs larger than 4x L2"
+    per_copy = sum(d[k].numel() * d[k].element_size() for k in INPUT_KEYS
+                   if d.get(k) is not None)
+    n = min(4096, max(3, -(-4 * L2_BYTES // nbytes) + 1))
+    n = max(3, min(n, (2 << 30) // max(per_copy, 1)))
+    copies = [d]
+    for _ in range(n - 1):
+        c = dict(d)
+        for k in INPUT_KEYS:
+            if d.get(k) is not None:
+                c[k] = d[k].clone()
+        copies.append(c)
+    return copies, (f"{n} rotating input copies ({n * per_copy / 2**20:.0f} MiB); each step "
+                    f"reads a copy last touched {n - 1} steps earlier (> 4x L2 read since)")
+
+
 def time_kernel(wl, d, steps, warmup, world, device, clocks_gpu=None):
     """Kernel-only timing.  Returns dict with per-step and split-kernel µs."""
     import torch
     from decode_step_kv_gb300 import binding
     from decode_step_kv_gb300.inputs import kv_bytes
     nbytes = kv_bytes(wl, d["lens"], None if d["window"] is None else d["window"].tolist())
-    flush = None
-    if nbytes < 4 * L2_BYTES:
-        flush = torch.empty(512 * 2 ** 20, dtype=torch.uint8, device=device)
+    copies, l2_note = rotation(d, nbytes)
+    R = len(copies)
     stream = torch.cuda.current_stream(device)
-    for _ in range(warmup):
-        if flush is not None:
-            flush.fill_(1)
-        call(wl, d, stream)
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
-           torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for i in range(warmup):
+        call(wl, copies[i % R], stream)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
     sampler = ClockSampler(clocks_gpu) if clocks_gpu is not None else None
     barrier(world)
     torch.cuda.synchronize(device)
@@ -210,29 +233,37 @@ def time_kernel(wl, d, steps, warmup, world, device, clocks_gpu=None):
         sampler.__enter__()
     t0 = time.perf_counter()
     for i in range(steps):
-        if flush is not None:
-            flush.fill_(i & 0xFF)
         ev[i][0].record(stream)
-        ev[i][1].record(stream)   # creates the event; the library re-records it after the split kernel
-        binding.fa_decode_profile_next(None, ev[i][1])
-        call(wl, d, stream)
-        ev[i][2].record(stream)
+        call(wl, copies[(warmup + i) % R], stream)
+        ev[i][1].record(stream)
     torch.cuda.synchronize(device)
     wall = time.perf_counter() - t0
     barrier(world)
     if sampler:
         sampler.__exit__()
-    step_ms = [a.elapsed_time(c) for a, _, c in ev]
-    split_ms = [a.elapsed_time(b) for a, b, _ in ev]
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    # second pass, same steps: the library records an event right after the
+    # split kernel (this pass is not the step timing: the event sits between
+    # the two kernels and stops the merge from overlapping the split's tail)
+    ev2 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    torch.cuda.synchronize(device)
+    for i in range(steps):
+        ev2[i][0].record(stream)
+        ev2[i][1].record(stream)   # creates the event; the library re-records it after the split
+        binding.fa_decode_profile_next(None, ev2[i][1])
+        call(wl, copies[(warmup + steps + i) % R], stream)
+    torch.cuda.synchronize(device)
+    split_ms = [a.elapsed_time(b) for a, b in ev2]
+    del copies
     res = {
         "us_per_step": 1e3 * statistics.mean(step_ms),
         "us_per_step_median": 1e3 * statistics.median(step_ms),
         "split_us": 1e3 * statistics.mean(split_ms),
         "kv_bytes": nbytes,
         "wall_s": wall,
-        "l2": ("flushed: 512 MiB written before each step" if flush is not None
-               else "inputs larger than 4x L2"),
-        "launches": 2 * steps,
+        "l2": l2_note,
+        "launches": 2 * steps,      # split + merge per timed step
     }
     if sampler:
         res["clocks"] = sampler.summary()

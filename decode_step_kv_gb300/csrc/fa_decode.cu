@@ -81,8 +81,11 @@ struct Params {
     long long cap;    // tokens per sequence
     float c2;         // scale * log2(e)
     int tile;         // tokens per tile
-    int tps;          // tiles per split
+    int tps;          // tiles per split (split kernels)
     int max_splits;
+    int W;            // stream-K workers (warps) in the grid
+    int U_b;          // units per sequence: kv heads x head groups
+    int sh;           // heads stored per workspace slot (stream-K)
 };
 
 // ------------------------------------------------------------ PTX wrappers
@@ -264,6 +267,8 @@ __global__ void __launch_bounds__(THREADS, 2) fa_split_kernel(const Params p)
     constexpr int NSC = TILE * GP;                 // scores per tile
     constexpr int NR = (NSC + 31) / 32;            // scores per lane in the softmax step
 
+    // let the merge grid launch early (it waits for this grid before reading)
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int z = blockIdx.x;
     const int kv = blockIdx.y / p.n_hg;
     const int hg = blockIdx.y % p.n_hg;
@@ -600,20 +605,28 @@ __global__ void __launch_bounds__(THREADS, 2) fa_split_kernel(const Params p)
 namespace tc {
 
 constexpr int TILE = 16;
-constexpr int NWARPS = 4;
-constexpr int GPH = 8;          // heads per CTA (the mma N dimension)
+constexpr int GPH = 8;          // heads per unit (the mma N dimension)
 
-template <int D>
+template <int D, bool VI8>
 struct Cfg {
+    // D=128: 4 warps x 3 stages (~100 KB, two CTAs per SM); D=256: 6 warps x
+    // 2 stages (~200 KB, one CTA per SM) so each scheduler has warps to switch to
+    static constexpr int NW = D == 128 ? 4 : 6;
     static constexpr int STAGES = D == 128 ? 3 : 2;
     static constexpr int BOXES = D / 64;                  // 64-column boxes per row
     static constexpr int BOX_BYTES = TILE * 128;          // 16 rows x 128 B
-    static constexpr int T_BYTES = BOXES * BOX_BYTES;     // one tensor's tile (K or V)
-    static constexpr int STAGE_BYTES = 2 * T_BYTES;
-    static constexpr int RING_BYTES = NWARPS * STAGES * STAGE_BYTES;
-    static constexpr int MERGE_BYTES = sizeof(float) * (NWARPS * GPH * D + 2 * NWARPS * GPH);
-    static constexpr int SMEM = (RING_BYTES > MERGE_BYTES ? RING_BYTES : MERGE_BYTES) +
-                                NWARPS * STAGES * 8 + 1024;   // + barriers + alignment slack
+    static constexpr int T_BYTES = BOXES * BOX_BYTES;     // one fp16 tile (K, or fp16 V)
+    static constexpr int V8_BYTES = TILE * D;             // int8 V tile
+    static constexpr int S_BYTES = TILE * (D / 32) * 2;   // its fp16 scales
+    static constexpr int V_STAGE = VI8 ? V8_BYTES + S_BYTES : T_BYTES;
+    static constexpr int TX_BYTES = T_BYTES + V_STAGE;    // bytes landing per stage
+    static constexpr int STAGE_BYTES = (TX_BYTES + 1023) / 1024 * 1024;
+    static constexpr int CVT_BYTES = VI8 ? T_BYTES : 0;   // per-warp dequantised V tile
+    static constexpr int WARP_BYTES = STAGES * STAGE_BYTES + CVT_BYTES;
+    static constexpr int RING_BYTES = NW * WARP_BYTES;
+    static constexpr int SMEM = RING_BYTES + NW * STAGES * 8 + 1024;   // + barriers + alignment
+    static constexpr int CTAS_PER_SM = D == 128 ? 2 : 1;
+    static_assert(CTAS_PER_SM * (SMEM + 1024) <= 228 * 1024, "shared memory per SM");
 };
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y,
@@ -665,6 +678,22 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi)
     return *reinterpret_cast<const uint32_t *>(&h);
 }
 
+// Four int8 codes -> two half2 of code * scale.  Each biased byte u = code +
+// 128 becomes the fp16 1024 + u by placing it under the exponent byte 0x64;
+// subtracting 1152 gives the code exactly, and one fp16 multiply by the scale
+// rounds the product once (code * scale has at most 18 significant bits).
+__device__ __forceinline__ void dequant4(uint32_t w, __half2 s2, uint32_t &lo, uint32_t &hi)
+{
+    const uint32_t u = w ^ 0x80808080u;
+    const uint32_t a = __byte_perm(u, 0x64646464u, 0x4140);
+    const uint32_t b = __byte_perm(u, 0x64646464u, 0x4342);
+    const __half2 bias = __half2half2(__ushort_as_half((unsigned short)0x6480));   // 1152
+    __half2 ha = __hmul2(__hsub2(*reinterpret_cast<const __half2 *>(&a), bias), s2);
+    __half2 hb = __hmul2(__hsub2(*reinterpret_cast<const __half2 *>(&b), bias), s2);
+    lo = *reinterpret_cast<const uint32_t *>(&ha);
+    hi = *reinterpret_cast<const uint32_t *>(&hb);
+}
+
 // Shared address of 16-byte chunk `chunk` (0..D/8-1) of tile row `row` in a
 // tile of BOXES swizzled 64-column boxes.
 __device__ __forceinline__ uint32_t swz(uint32_t base, int row, int chunk)
@@ -687,40 +716,155 @@ __device__ __forceinline__ long long tile_row(const Params &p, int b, int kv, in
     return ((long long)b * p.Hkv + kv) * p.cap + tok;
 }
 
-template <int D>
-__global__ void __launch_bounds__(NWARPS * 32, 1)
-    fa_split_mma_kernel(const Params p, const __grid_constant__ CUtensorMap tmK,
-                        const __grid_constant__ CUtensorMap tmV)
+// Per-sequence walk over the flattened tile space.  Units (one KV head and
+// head group of one sequence) are ordered by (sequence, unit); the tiles of
+// a unit are its 16-token tiles intersecting the attended range [lo, hi).
+struct Walk {
+    int b, j, k, n, lo, hi;   // sequence, unit in sequence, tile in unit, tiles per unit
+    long long P;              // flattened index of sequence b's first tile
+
+    __device__ __forceinline__ void load(const Params &p)
+    {
+        attended_range(p, b, lo, hi, false);
+        n = tiles_in<TILE>(lo, hi);
+    }
+    // position at flattened tile t of sequence b_ (whose first tile is P_)
+    __device__ __forceinline__ void init(const Params &p, int b_, long long P_, long long t)
+    {
+        b = b_;
+        P = P_;
+        load(p);
+        const long long off = t - P;
+        j = static_cast<int>(off / n);
+        k = static_cast<int>(off % n);
+    }
+    __device__ __forceinline__ void next(const Params &p)
+    {
+        if (++k < n)
+            return;
+        k = 0;
+        if (++j < p.U_b)
+            return;
+        j = 0;
+        do {
+            P += (long long)p.U_b * n;
+            ++b;
+            if (b >= p.B)
+                return;
+            load(p);
+        } while (n == 0);
+    }
+    __device__ __forceinline__ int tok() const { return (lo / TILE + k) * TILE; }
+    __device__ __forceinline__ long long unit(const Params &p) const
+    {
+        return (long long)b * p.U_b + j;
+    }
+    __device__ __forceinline__ long long unit_start() const { return P + (long long)j * n; }
+};
+
+// Warp-cooperative scan over the sequences: T = all tiles of the step; when
+// target >= 0 also the sequence holding flattened tile `target` and that
+// sequence's first flattened tile.  Every lane returns the same values.
+__device__ __forceinline__ long long flat_scan(const Params &p, long long target, int &b_at,
+                                               long long &P_at, bool report = false)
 {
-    using C = Cfg<D>;
+    const int lane = threadIdx.x & 31;
+    long long run = 0;
+    b_at = -1;
+    P_at = 0;
+    for (int b0 = 0; b0 < p.B; b0 += 32) {
+        const int b = b0 + lane;
+        long long c = 0;
+        if (b < p.B) {
+            int lo, hi;
+            attended_range(p, b, lo, hi, report);
+            c = (long long)tiles_in<TILE>(lo, hi) * p.U_b;
+        }
+        long long x = c;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const long long y = __shfl_up_sync(0xffffffffu, x, off);
+            if (lane >= off)
+                x += y;
+        }
+        const long long excl = run + x - c;
+        if (target >= 0 && b_at < 0) {
+            const unsigned hit = __ballot_sync(0xffffffffu, b < p.B && target >= excl &&
+                                                                target < excl + c);
+            if (hit) {
+                const int src = __ffs(hit) - 1;
+                b_at = b0 + src;
+                P_at = __shfl_sync(0xffffffffu, excl, src);
+            }
+        }
+        run += __shfl_sync(0xffffffffu, x, 31);
+    }
+    return run;
+}
+
+// Workers actually used for T tiles (at least MIN_TPW tiles each), and the
+// worker whose contiguous range holds flattened tile t.
+constexpr int MIN_TPW = 1;
+__device__ __forceinline__ int workers_for(const Params &p, long long T)
+{
+    long long w = T / MIN_TPW;
+    if (w < 1)
+        w = 1;
+    return static_cast<int>(w < p.W ? w : p.W);
+}
+__device__ __forceinline__ long long range_start(long long w, long long T, int We)
+{
+    return w * T / We;
+}
+__device__ __forceinline__ int worker_of(long long t, long long T, int We)
+{
+    return static_cast<int>(((t + 1) * We - 1) / T);
+}
+
+// Persistent stream-K split kernel on the tensor cores.  Every warp is an
+// independent worker: worker w streams the flattened tiles
+// [w*T/We, (w+1)*T/We) through its own TMA ring, crossing unit boundaries
+// without a pause.  At the end of each unit segment it writes either the
+// normalised output (the unit lies wholly in its range) or a partial
+// (O, m, l) to workspace slot w + unit (unique: the workers covering
+// consecutive units are non-decreasing).  The merge kernel folds the slots.
+template <int D, bool VI8>
+__global__ void __launch_bounds__(Cfg<D, VI8>::NW * 32, 1)
+    fa_stream_mma_kernel(const Params p, const __grid_constant__ CUtensorMap tmK,
+                         const __grid_constant__ CUtensorMap tmV)
+{
+    using C = Cfg<D, VI8>;
     constexpr int STAGES = C::STAGES;
     constexpr int KS = D / 16;                       // k-steps of QK, m-tiles of PV
 
-    const int z = blockIdx.x;
-    const int kv = blockIdx.y / p.n_hg;
-    const int hg = blockIdx.y % p.n_hg;
-    const int b = blockIdx.z;
-
-    int lo, hi;
-    attended_range(p, b, lo, hi, z == 0 && blockIdx.y == 0 && threadIdx.x == 0);
-    const int nt = tiles_in<TILE>(lo, hi);
-    const int n_splits = (nt + p.tps - 1) / p.tps;
-    if (z >= n_splits)
-        return;
-    const int t_first = lo / TILE + z * p.tps;
-    const int t_count = min(p.tps, nt - z * p.tps);
-
-    extern __shared__ unsigned char smem_raw[];
-    unsigned char *smem = reinterpret_cast<unsigned char *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t *bars = reinterpret_cast<uint64_t *>(
-        smem + (C::RING_BYTES > C::MERGE_BYTES ? C::RING_BYTES : C::MERGE_BYTES));
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int g4 = lane >> 2;        // fragment row group
     const int t4 = lane & 3;         // fragment column pair
-    const uint32_t ring = smem_u32(smem) + warp * STAGES * C::STAGE_BYTES;
+    const int w = blockIdx.x * C::NW + warp;
+
+    int b_at;
+    long long P_at;
+    // worker 0 also reports lengths clamped to the capacity
+    const long long T = flat_scan(p, -1, b_at, P_at, w == 0);
+    if (T == 0)
+        return;
+    const int We = workers_for(p, T);
+    if (w >= We)
+        return;
+    const long long t0 = range_start(w, T, We);
+    const long long t1 = range_start(w + 1, T, We);
+    const int n_my = static_cast<int>(t1 - t0);
+    flat_scan(p, t0, b_at, P_at);
+
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char *smem = reinterpret_cast<unsigned char *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::RING_BYTES);
+    const uint32_t ring = smem_u32(smem) + warp * C::WARP_BYTES;
+    const uint32_t cvt = ring + STAGES * C::STAGE_BYTES;     // int8 V: dequantised tile
     const uint32_t my_bars = smem_u32(bars + warp * STAGES);
 
     if (lane == 0)
@@ -729,79 +873,149 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     __syncwarp();
 
-    const int nh = min(GPH, p.G - hg * GPH);         // real heads in this CTA
-    // Q^T as the QK B operand: b0 = q[head g4][16ks + 2t4 .. +1], b1 = +8
-    uint32_t qb[KS][2];
-    {
-        const bool live = g4 < nh;
-        const __half *qrow = p.q + ((long long)b * p.Hq + kv * p.G + hg * GPH + g4) * D;
-#pragma unroll
-        for (int ks = 0; ks < KS; ++ks) {
-            qb[ks][0] = live ? *reinterpret_cast<const uint32_t *>(qrow + ks * 16 + 2 * t4) : 0u;
-            qb[ks][1] = live ? *reinterpret_cast<const uint32_t *>(qrow + ks * 16 + 8 + 2 * t4)
-                             : 0u;
-        }
-    }
-
-    float acc[KS][4];
-#pragma unroll
-    for (int i = 0; i < KS; ++i)
-        acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
-    float m0 = -INFINITY, m1 = -INFINITY;    // running max, heads 2t4 and 2t4+1
-    float l0 = 0.f, l1 = 0.f;                // this lane's share of the sums
-
     const uint64_t policy = evict_first_policy();
-    const int n_my = t_count > warp ? (t_count - warp + NWARPS - 1) / NWARPS : 0;
+    Walk pw;                          // producer position (lane 0 issues)
+    pw.init(p, b_at, P_at, t0);
+    Walk cw = pw;                     // consumer position
 
-    auto issue = [&](int j, int s) {
-        const int ti = t_first + warp + j * NWARPS;
+    auto issue = [&](int s) {
         const uint32_t bar = my_bars + 8 * s;
-        const long long row = tile_row(p, b, kv, ti * TILE);
+        const int kv = pw.j / p.n_hg;
+        const long long row = tile_row(p, pw.b, kv, pw.tok());
         if (row < 0) {
             flag(FA_STATUS_BAD_BLOCK);
             mbar_expect_tx(bar, 0);
             return;
         }
-        mbar_expect_tx(bar, C::STAGE_BYTES);
+        mbar_expect_tx(bar, C::TX_BYTES);
         const uint32_t st = ring + s * C::STAGE_BYTES;
 #pragma unroll
         for (int bx = 0; bx < C::BOXES; ++bx) {
             tma_load_2d(st + bx * C::BOX_BYTES, &tmK, bx * 64, (int)row, bar, policy);
-            tma_load_2d(st + C::T_BYTES + bx * C::BOX_BYTES, &tmV, bx * 64, (int)row, bar,
-                        policy);
+            if constexpr (!VI8)
+                tma_load_2d(st + C::T_BYTES + bx * C::BOX_BYTES, &tmV, bx * 64, (int)row, bar,
+                            policy);
+        }
+        if constexpr (VI8) {
+            // the tile's 16 int8 rows and their scale rows are contiguous
+            bulk_g2s(st + C::T_BYTES, p.v + row * D, C::V8_BYTES, bar, policy);
+            bulk_g2s(st + C::T_BYTES + C::V8_BYTES, p.vs + row * (D / 32) * 2, C::S_BYTES, bar,
+                     policy);
         }
     };
 
-    if (lane == 0)
-        for (int j = 0; j < STAGES && j < n_my; ++j)
-            issue(j, j);
+    const int n_pre = n_my < STAGES ? n_my : STAGES;
+    for (int s = 0; s < n_pre; ++s) {
+        if (lane == 0)
+            issue(s);
+        pw.next(p);
+    }
     __syncwarp();
 
-    int j_fail = -1;
-    for (int j = 0; j < n_my; ++j) {
-        const int s = j % STAGES;
-        if (!mbar_wait_warp(my_bars + 8 * s, (j / STAGES) & 1)) {
+    // Q^T of the current unit as the QK B operand: b0 = q[head g4][16ks+2t4..], b1 = +8
+    uint32_t qb[KS][2];
+    int nh = 0;
+    auto load_q = [&](const Walk &u) {
+        const int kv = u.j / p.n_hg;
+        const int hg = u.j % p.n_hg;
+        nh = min(GPH, p.G - hg * GPH);
+        const bool live = g4 < nh;
+        const __half *qrow = p.q + ((long long)u.b * p.Hq + kv * p.G + hg * GPH + g4) * D;
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+            qb[ks][0] = live ? __ldg(reinterpret_cast<const unsigned *>(qrow + ks * 16 + 2 * t4))
+                             : 0u;
+            qb[ks][1] =
+                live ? __ldg(reinterpret_cast<const unsigned *>(qrow + ks * 16 + 8 + 2 * t4)) : 0u;
+        }
+    };
+    load_q(cw);
+    // pull a unit's query rows into L2 when its first tile is issued, so the
+    // switch to that unit does not wait on HBM
+    auto prefetch_q = [&](const Walk &u) {
+        const int kv = u.j / p.n_hg;
+        const int hg = u.j % p.n_hg;
+        const int nq = min(GPH, p.G - hg * GPH);
+        const char *base = reinterpret_cast<const char *>(
+            p.q + ((long long)u.b * p.Hq + kv * p.G + hg * GPH) * D);
+        if (lane * 128 < nq * D * 2)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(base + lane * 128));
+    };
+
+    float acc[KS][4];
+    float m0, m1, l0, l1;
+    auto reset = [&] {
+#pragma unroll
+        for (int i = 0; i < KS; ++i)
+            acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+        m0 = m1 = -INFINITY;
+        l0 = l1 = 0.f;
+    };
+    reset();
+
+    int i_fail = -1;
+    for (int i = 0; i < n_my; ++i) {
+        const int s = i % STAGES;
+        if (!mbar_wait_warp(my_bars + 8 * s, (i / STAGES) & 1)) {
             if (lane == 0)
                 flag(FA_STATUS_WAIT_TIMEOUT);
-            j_fail = j;
+            i_fail = i;
             break;
         }
-        const int ti = t_first + warp + j * NWARPS;
-        const int base = ti * TILE;
-        const int r0 = max(lo - base, 0);
-        const int r1 = min(hi - base, TILE);
-        const bool block_ok = tile_row(p, b, kv, base) >= 0;
+        const int kv = cw.j / p.n_hg;
+        const int base = cw.tok();
+        const int r0 = max(cw.lo - base, 0);
+        const int r1 = min(cw.hi - base, TILE);
+        const bool block_ok = tile_row(p, cw.b, kv, base) >= 0;
         const uint32_t sK = ring + s * C::STAGE_BYTES;
-        const uint32_t sV = sK + C::T_BYTES;
+        const uint32_t sV = VI8 ? cvt : sK + C::T_BYTES;
 
         if (block_ok) {
-            if (r0 != 0 || r1 != TILE) {
+            if constexpr (VI8) {
+                // dequantise the int8 tile into the warp's fp16 tile (same
+                // swizzled layout as a TMA-loaded one); keys outside [r0, r1)
+                // become zero rows
+                constexpr int CPR = D / 16;               // 16-code chunks per row
+                const uint32_t v8 = sK + C::T_BYTES;
+                const uint32_t sc = v8 + C::V8_BYTES;
+#pragma unroll
+                for (int kk = 0; kk < TILE * CPR / 32; ++kk) {
+                    const int q = lane + 32 * kk;
+                    const int row = q / CPR;
+                    const int cc = q % CPR;
+                    uint32_t o[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+                    if (row >= r0 && row < r1) {
+                        uint32_t w0, w1, w2, w3;
+                        unsigned short sb;
+                        asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                                     : "=r"(w0), "=r"(w1), "=r"(w2), "=r"(w3)
+                                     : "r"(v8 + row * D + cc * 16));
+                        asm volatile("ld.shared.u16 %0, [%1];"
+                                     : "=h"(sb)
+                                     : "r"(sc + (row * (D / 32) + cc / 2) * 2));
+                        const __half2 s2 = __half2half2(__ushort_as_half(sb));
+                        dequant4(w0, s2, o[0], o[1]);
+                        dequant4(w1, s2, o[2], o[3]);
+                        dequant4(w2, s2, o[4], o[5]);
+                        dequant4(w3, s2, o[6], o[7]);
+                    }
+                    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(
+                                     swz(cvt, row, 2 * cc)),
+                                 "r"(o[0]), "r"(o[1]), "r"(o[2]), "r"(o[3])
+                                 : "memory");
+                    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(
+                                     swz(cvt, row, 2 * cc + 1)),
+                                 "r"(o[4]), "r"(o[5]), "r"(o[6]), "r"(o[7])
+                                 : "memory");
+                }
+                __syncwarp();
+            } else if (r0 != 0 || r1 != TILE) {
                 // keys outside [r0, r1) hold other tokens' data: zero their V
                 // rows (a 128-byte row segment per box) so 0-weights stay 0
-                for (int i = lane; i < TILE * C::BOXES * 8; i += 32) {
-                    const int row = i / (C::BOXES * 8);
+                for (int ii = lane; ii < TILE * C::BOXES * 8; ii += 32) {
+                    const int row = ii / (C::BOXES * 8);
                     if (row < r0 || row >= r1) {
-                        const int rem = i % (C::BOXES * 8);
+                        const int rem = ii % (C::BOXES * 8);
                         const uint32_t a = sV + (rem >> 3) * C::BOX_BYTES + row * 128 +
                                            (rem & 7) * 16;
                         asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(a), "r"(0)
@@ -811,27 +1025,34 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 __syncwarp();
             }
-            // ---- S = K . Q^T  (rows: keys g4, g4+8; cols: heads 2t4, 2t4+1)
-            float sc[4] = {0.f, 0.f, 0.f, 0.f};
+            // ---- S = K . Q^T  (rows: keys g4, g4+8; cols: heads 2t4, 2t4+1),
+            // even and odd k-steps in two accumulators to halve the mma chain
+            float sc4[4] = {0.f, 0.f, 0.f, 0.f};
             {
+                float sc4b[4] = {0.f, 0.f, 0.f, 0.f};
                 const int mi = lane >> 3;
                 const int krow = (mi & 1) * 8 + (lane & 7);
 #pragma unroll
-                for (int ks = 0; ks < KS; ++ks) {
-                    uint32_t a0, a1, a2, a3;
+                for (int ks = 0; ks < KS; ks += 2) {
+                    uint32_t a0, a1, a2, a3, e0, e1, e2, e3;
                     ldsm_x4(swz(sK, krow, ks * 2 + (mi >> 1)), a0, a1, a2, a3);
-                    mma16816(sc, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
+                    ldsm_x4(swz(sK, krow, ks * 2 + 2 + (mi >> 1)), e0, e1, e2, e3);
+                    mma16816(sc4, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
+                    mma16816(sc4b, e0, e1, e2, e3, qb[ks + 1][0], qb[ks + 1][1]);
                 }
+#pragma unroll
+                for (int r = 0; r < 4; ++r)
+                    sc4[r] += sc4b[r];
             }
             const bool va = g4 >= r0 && g4 < r1;
             const bool vb = g4 + 8 >= r0 && g4 + 8 < r1;
-            sc[0] = va ? sc[0] * p.c2 : -INFINITY;
-            sc[1] = va ? sc[1] * p.c2 : -INFINITY;
-            sc[2] = vb ? sc[2] * p.c2 : -INFINITY;
-            sc[3] = vb ? sc[3] * p.c2 : -INFINITY;
+            sc4[0] = va ? sc4[0] * p.c2 : -INFINITY;
+            sc4[1] = va ? sc4[1] * p.c2 : -INFINITY;
+            sc4[2] = vb ? sc4[2] * p.c2 : -INFINITY;
+            sc4[3] = vb ? sc4[3] * p.c2 : -INFINITY;
             // ---- online softmax per head (lanes sharing t4 share the heads)
-            float x0 = fmaxf(sc[0], sc[2]);
-            float x1 = fmaxf(sc[1], sc[3]);
+            float x0 = fmaxf(sc4[0], sc4[2]);
+            float x1 = fmaxf(sc4[1], sc4[3]);
 #pragma unroll
             for (int mask = 4; mask <= 16; mask <<= 1) {
                 x0 = fmaxf(x0, __shfl_xor_sync(0xffffffffu, x0, mask));
@@ -843,19 +1064,19 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
                 const float a0 = ex2(m0 - n0);
                 const float a1 = ex2(m1 - n1);
 #pragma unroll
-                for (int i = 0; i < KS; ++i) {
-                    acc[i][0] *= a0;
-                    acc[i][1] *= a1;
-                    acc[i][2] *= a0;
-                    acc[i][3] *= a1;
+                for (int ii = 0; ii < KS; ++ii) {
+                    acc[ii][0] *= a0;
+                    acc[ii][1] *= a1;
+                    acc[ii][2] *= a0;
+                    acc[ii][3] *= a1;
                 }
                 l0 *= a0;
                 l1 *= a1;
                 m0 = n0;
                 m1 = n1;
             }
-            const float p0 = ex2(sc[0] - m0), p1 = ex2(sc[1] - m1);
-            const float p2 = ex2(sc[2] - m0), p3 = ex2(sc[3] - m1);
+            const float p0 = ex2(sc4[0] - m0), p1 = ex2(sc4[1] - m1);
+            const float p2 = ex2(sc4[2] - m0), p3 = ex2(sc4[3] - m1);
             l0 += p0 + p2;
             l1 += p1 + p3;
             // ---- P^T as the PV B operand (keys x heads), via movmatrix
@@ -874,65 +1095,221 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
             }
         }
         __syncwarp();
-        if (lane == 0 && j + STAGES < n_my)
-            issue(j + STAGES, s);
+        if (i + STAGES < n_my) {
+            if (pw.k == 0)
+                prefetch_q(pw);
+            if (lane == 0)
+                issue(s);
+            pw.next(p);
+        }
         __syncwarp();
-    }
-    if (j_fail >= 0)
-        for (int jj = j_fail; jj < n_my && jj < j_fail + STAGES; ++jj)
-            mbar_wait_warp(my_bars + 8 * (jj % STAGES), (jj / STAGES) & 1);
 
-    // ---- warp epilogue: complete the sums, publish (O, m, l) per head
+        if (cw.k == cw.n - 1 || i == n_my - 1) {
+            // ---- end of this worker's segment of the unit: publish it
 #pragma unroll
-    for (int mask = 4; mask <= 16; mask <<= 1) {
-        l0 += __shfl_xor_sync(0xffffffffu, l0, mask);
-        l1 += __shfl_xor_sync(0xffffffffu, l1, mask);
-    }
-    __syncthreads();                                  // every warp done with the ring
-    float *ow = reinterpret_cast<float *>(smem);      // [NWARPS][GPH][D]
-    float *mw = ow + NWARPS * GPH * D;                // [NWARPS][GPH]
-    float *lw = mw + NWARPS * GPH;
+            for (int mask = 4; mask <= 16; mask <<= 1) {
+                l0 += __shfl_xor_sync(0xffffffffu, l0, mask);
+                l1 += __shfl_xor_sync(0xffffffffu, l1, mask);
+            }
+            const long long us = cw.unit_start();
+            const int wf = worker_of(us, T, We);
+            const int wl = worker_of(us + cw.n - 1, T, We);
+            const int hbase = (cw.j / p.n_hg) * p.G + (cw.j % p.n_hg) * GPH;
+            const int h0 = 2 * t4, h1 = 2 * t4 + 1;
+            if (wf == wl) {
+                // the whole unit was ours: normalised output
+                const float i0 = l0 > 0.f ? 1.f / l0 : 0.f;
+                const float i1 = l1 > 0.f ? 1.f / l1 : 0.f;
+                float *o = p.out + ((long long)cw.b * p.Hq + hbase) * D;
 #pragma unroll
-    for (int mt = 0; mt < KS; ++mt) {
-        float *o = ow + (warp * GPH + 2 * t4) * D + mt * 16 + g4;
-        o[0] = acc[mt][0];
-        o[D] = acc[mt][1];
-        o[8] = acc[mt][2];
-        o[D + 8] = acc[mt][3];
+                for (int mt = 0; mt < KS; ++mt) {
+                    const int d = mt * 16 + g4;
+                    if (h0 < nh) {
+                        o[h0 * D + d] = acc[mt][0] * i0;
+                        o[h0 * D + d + 8] = acc[mt][2] * i0;
+                    }
+                    if (h1 < nh) {
+                        o[h1 * D + d] = acc[mt][1] * i1;
+                        o[h1 * D + d + 8] = acc[mt][3] * i1;
+                    }
+                }
+            } else {
+                const long long slot = w + cw.unit(p);
+                float *o = p.ws_o + slot * p.sh * D;
+#pragma unroll
+                for (int mt = 0; mt < KS; ++mt) {
+                    const int d = mt * 16 + g4;
+                    if (h0 < nh) {
+                        o[h0 * D + d] = acc[mt][0];
+                        o[h0 * D + d + 8] = acc[mt][2];
+                    }
+                    if (h1 < nh) {
+                        o[h1 * D + d] = acc[mt][1];
+                        o[h1 * D + d + 8] = acc[mt][3];
+                    }
+                }
+                if (g4 == 0) {
+                    if (h0 < nh)
+                        p.ws_ml[slot * p.sh + h0] = make_float2(m0, l0);
+                    if (h1 < nh)
+                        p.ws_ml[slot * p.sh + h1] = make_float2(m1, l1);
+                }
+            }
+            reset();
+            if (i + 1 < n_my) {
+                cw.next(p);
+                load_q(cw);
+            }
+        } else {
+            cw.next(p);
+        }
     }
-    if (g4 == 0) {
-        mw[warp * GPH + 2 * t4] = m0;
-        mw[warp * GPH + 2 * t4 + 1] = m1;
-        lw[warp * GPH + 2 * t4] = l0;
-        lw[warp * GPH + 2 * t4 + 1] = l1;
+    if (i_fail >= 0)
+        for (int ii = i_fail; ii < n_my && ii < i_fail + STAGES; ++ii)
+            mbar_wait_warp(my_bars + 8 * (ii % STAGES), (ii / STAGES) & 1);
+}
+
+// Log-sum-exp merge for the stream-K kernel: one CTA of MERGE_THREADS per
+// (sequence, query head) row folds the partial slots of the workers that
+// covered the row's unit (or writes the zero row of an empty range).  The
+// slots are spread over the threads: each thread owns one float4 column of
+// D and a strided subset of the slots, so the loads of many slots are in
+// flight at once; the per-slot weights ex2(m - M) are computed once into
+// shared memory.
+constexpr int MERGE_THREADS = 256;
+constexpr int MERGE_MAX_SLOTS = 512;   // per pass over the slots
+
+template <int D>
+__global__ void __launch_bounds__(MERGE_THREADS) fa_stream_merge_kernel(const Params p)
+{
+    constexpr int CH = D / 4;                    // float4 columns
+    constexpr int SG = MERGE_THREADS / CH;       // slot groups
+    __shared__ float wgt[MERGE_MAX_SLOTS];
+    __shared__ float red[MERGE_THREADS / 32];
+    __shared__ float4 part[SG][CH];
+
+    const long long row = blockIdx.x;
+    const int b = static_cast<int>(row / p.Hq);
+    const int h = static_cast<int>(row % p.Hq);
+    const int kv = h / p.G;
+    const int gi = h % p.G;
+    const int j = kv * p.n_hg + gi / GPH;
+    const int hh = gi % GPH;
+    const int tid = threadIdx.x;
+    const int lane = tid & 31, wid = tid >> 5;
+
+    int lo, hi;
+    attended_range(p, b, lo, hi, false);
+    const int n = tiles_in<TILE>(lo, hi);
+    if (n == 0) {
+        if (tid < CH)
+            reinterpret_cast<float4 *>(p.out + row * D)[tid] = make_float4(0.f, 0.f, 0.f, 0.f);
+        return;
+    }
+    // T and the flattened start of sequence b (warp 0 scans; all warps then
+    // read the results from shared memory)
+    __shared__ long long sh_T, sh_P;
+    if (wid == 0) {
+        int b_at;
+        long long P_at;
+        const long long T = flat_scan(p, -1, b_at, P_at);
+        long long run = 0;
+        for (int b0 = 0; b0 < b; b0 += 32) {
+            const int bb = b0 + lane;
+            long long c = 0;
+            if (bb < b) {
+                int l2, h2;
+                attended_range(p, bb, l2, h2, false);
+                c = (long long)tiles_in<TILE>(l2, h2) * p.U_b;
+            }
+#pragma unroll
+            for (int off = 16; off >= 1; off >>= 1)
+                c += __shfl_xor_sync(0xffffffffu, c, off);
+            run += c;
+        }
+        if (lane == 0) {
+            sh_T = T;
+            sh_P = run;
+        }
     }
     __syncthreads();
+    const long long T = sh_T;
+    const int We = workers_for(p, T);
+    const long long us = sh_P + (long long)j * n;
+    const int wf = worker_of(us, T, We);
+    const int wl = worker_of(us + n - 1, T, We);
+    if (wf == wl)
+        return;                                   // written by the split kernel
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const long long u = (long long)b * p.U_b + j;
+    const int ns = wl - wf + 1;
 
-    for (int idx = threadIdx.x; idx < nh * D; idx += NWARPS * 32) {
-        const int g = idx / D;
-        const int d = idx % D;
-        float M = -INFINITY;
+    // pass 1: global max of the slots' running maxima
+    float M = -INFINITY;
+    for (int s = tid; s < ns; s += MERGE_THREADS)
+        M = fmaxf(M, p.ws_ml[(wf + s + u) * p.sh + hh].x);
 #pragma unroll
-        for (int w = 0; w < NWARPS; ++w)
-            M = fmaxf(M, mw[w * GPH + g]);
-        float L = 0.f, O = 0.f;
-        if (M != -INFINITY) {
+    for (int off = 16; off >= 1; off >>= 1)
+        M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    if (lane == 0)
+        red[wid] = M;
+    __syncthreads();
+    M = red[0];
 #pragma unroll
-            for (int w = 0; w < NWARPS; ++w) {
-                const float mwv = mw[w * GPH + g];
-                const float a = (mwv == -INFINITY) ? 0.f : ex2(mwv - M);
-                L = fmaf(lw[w * GPH + g], a, L);
-                O = fmaf(ow[(w * GPH + g) * D + d], a, O);
-            }
+    for (int i = 1; i < MERGE_THREADS / 32; ++i)
+        M = fmaxf(M, red[i]);
+    __syncthreads();
+
+    float L = 0.f;
+    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+    const int c = tid % CH;
+    const int sg = tid / CH;
+    for (int s0 = 0; s0 < ns; s0 += MERGE_MAX_SLOTS) {
+        const int cnt = min(MERGE_MAX_SLOTS, ns - s0);
+        // weights of this pass's slots, and their share of the sum
+        float Lp = 0.f;
+        for (int s = tid; s < cnt; s += MERGE_THREADS) {
+            const float2 v = p.ws_ml[(wf + s0 + s + u) * p.sh + hh];
+            const float a = (v.x == -INFINITY) ? 0.f : ex2(v.x - M);
+            wgt[s] = a;
+            Lp = fmaf(v.y, a, Lp);
         }
-        const long long row = (long long)b * p.Hq + kv * p.G + hg * GPH + g;
-        if (n_splits == 1) {
-            p.out[row * D + d] = L > 0.f ? O / L : 0.f;
-        } else {
-            p.ws_o[(row * p.max_splits + z) * D + d] = O;
-            if (d == 0)
-                p.ws_ml[row * p.max_splits + z] = make_float2(M, L);
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1)
+            Lp += __shfl_xor_sync(0xffffffffu, Lp, off);
+        if (lane == 0)
+            red[wid] = Lp;
+        __syncthreads();
+#pragma unroll
+        for (int i = 0; i < MERGE_THREADS / 32; ++i)
+            L += red[i];
+#pragma unroll 4
+        for (int s = sg; s < cnt; s += SG) {
+            const long long slot = wf + s0 + s + u;
+            const float4 x =
+                reinterpret_cast<const float4 *>(p.ws_o + (slot * p.sh + hh) * D)[c];
+            const float a = wgt[s];
+            o.x = fmaf(x.x, a, o.x);
+            o.y = fmaf(x.y, a, o.y);
+            o.z = fmaf(x.z, a, o.z);
+            o.w = fmaf(x.w, a, o.w);
         }
+        __syncthreads();
+    }
+    part[sg][c] = o;
+    __syncthreads();
+    if (sg == 0) {
+#pragma unroll
+        for (int g = 1; g < SG; ++g) {
+            const float4 y = part[g][c];
+            o.x += y.x;
+            o.y += y.y;
+            o.z += y.z;
+            o.w += y.w;
+        }
+        const float inv = L > 0.f ? 1.f / L : 0.f;
+        reinterpret_cast<float4 *>(p.out + row * D)[c] =
+            make_float4(o.x * inv, o.y * inv, o.z * inv, o.w * inv);
     }
 }
 
@@ -955,18 +1332,23 @@ __global__ void __launch_bounds__(D / 4) fa_merge_kernel(const Params p)
         *dst = make_float4(0.f, 0.f, 0.f, 0.f);
         return;
     }
+    // launched programmatically: wait here until the split grid's partials are visible
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const float2 *ml = p.ws_ml + row * p.max_splits;
+    const float4 *po = reinterpret_cast<const float4 *>(p.ws_o + row * p.max_splits * D) +
+                       threadIdx.x;
     float M = -INFINITY;
+#pragma unroll 8
     for (int s = 0; s < ns; ++s)
         M = fmaxf(M, ml[s].x);
     float L = 0.f;
     float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
     for (int s = 0; s < ns; ++s) {
         const float2 v = ml[s];
+        const float4 x = po[s * (D / 4)];
         const float a = (v.x == -INFINITY) ? 0.f : ex2(v.x - M);
         L = fmaf(v.y, a, L);
-        const float4 x = reinterpret_cast<const float4 *>(p.ws_o + (row * p.max_splits + s) * D)
-            [threadIdx.x];
         o.x = fmaf(x.x, a, o.x);
         o.y = fmaf(x.y, a, o.y);
         o.z = fmaf(x.z, a, o.z);
@@ -1046,10 +1428,14 @@ enum class Path { Simt, Mma };
 
 struct Plan {
     Path path;
+    int ctas;        // stream-K: persistent CTAs
+    int W;           // stream-K: warps (workers)
+    int sh;          // stream-K: heads per slot
     int tile;        // tokens per tile
     int gp;          // padded heads per CTA
     int hpg;         // real heads per CTA
     int n_hg;        // head groups per KV head
+    int units;       // units per sequence (kv heads x head groups)
     int tps;         // tiles per split
     int max_splits;
 };
@@ -1062,13 +1448,15 @@ static int next_pow2(int x)
     return p;
 }
 
-// Which split kernel serves a call: the tensor-core kernel for fp16 V, the
-// CUDA-core kernel for int8 V.  FA_DECODE_KERNEL=simt|mma overrides (for A/B
-// measurements); both compute the same result within the tolerances.
+// Which split kernel serves a call: the tensor-core kernel, unless
+// FA_DECODE_KERNEL=simt selects the CUDA-core one (for A/B measurements; both
+// compute the same result within the tolerances) or the cache is too large
+// for 32-bit TMA row coordinates.
 static Path choose_path(bool vi8)
 {
+    (void)vi8;
     const char *e = getenv("FA_DECODE_KERNEL");
-    if (vi8 || (e && !strcmp(e, "simt")))
+    if (e && !strcmp(e, "simt"))
         return Path::Simt;
     return Path::Mma;
 }
@@ -1078,7 +1466,7 @@ static Path choose_path(bool vi8)
 // here from the SM count rather than a fixed bucket).
 static Plan make_plan(Path path, int B, int Hq, int Hkv, int D, long long cap, int num_sms)
 {
-    Plan pl;
+    Plan pl = {};
     pl.path = path;
     const int G = Hq / Hkv;
     int ctas_per_sm;
@@ -1087,7 +1475,15 @@ static Plan make_plan(Path path, int B, int Hq, int Hkv, int D, long long cap, i
         pl.gp = tc::GPH;
         pl.hpg = tc::GPH;
         pl.n_hg = (G + tc::GPH - 1) / tc::GPH;
-        ctas_per_sm = D == 128 ? 2 : 1;
+        pl.sh = G < tc::GPH ? G : tc::GPH;
+        pl.units = Hkv * pl.n_hg;
+        const int nw = D == 128 ? tc::Cfg<128, false>::NW : tc::Cfg<256, false>::NW;
+        pl.ctas = (num_sms > 0 ? num_sms : 1) *
+                  (D == 128 ? tc::Cfg<128, false>::CTAS_PER_SM : tc::Cfg<256, false>::CTAS_PER_SM);
+        pl.W = pl.ctas * nw;
+        pl.tps = 0;
+        pl.max_splits = 0;
+        return pl;
     } else {
         pl.tile = 2048 / D;
         const int gpmax = D == 128 ? 4 : 2;
@@ -1117,6 +1513,12 @@ static Plan make_plan(Path path, int B, int Hq, int Hkv, int D, long long cap, i
 
 static size_t plan_workspace(const Plan &pl, int B, int Hq, int D)
 {
+    if (pl.path == Path::Mma) {
+        // partial slots: one per (worker, unit) pair, at most W + units
+        (void)Hq;
+        const size_t slots = (size_t)pl.W + (size_t)B * pl.units;
+        return slots * pl.sh * (D * sizeof(float) + sizeof(float2));
+    }
     if (pl.max_splits <= 1)
         return 0;
     const size_t rows = (size_t)B * Hq * pl.max_splits;
@@ -1227,11 +1629,11 @@ static int encode_kv_map(CUtensorMap *map, const void *base, long long rows, int
     return 0;
 }
 
-template <int D>
+template <int D, bool VI8>
 static cudaError_t launch_mma(const Params &p, const CUtensorMap &tmK, const CUtensorMap &tmV,
                               dim3 grid, cudaStream_t st)
 {
-    const int smem = tc::Cfg<D>::SMEM;
+    const int smem = tc::Cfg<D, VI8>::SMEM;
     static std::mutex mu;
     static bool done[64] = {false};
     int dev = 0;
@@ -1241,7 +1643,7 @@ static cudaError_t launch_mma(const Params &p, const CUtensorMap &tmK, const CUt
     {
         std::lock_guard<std::mutex> lock(mu);
         if (dev >= 64 || !done[dev]) {
-            e = cudaFuncSetAttribute(tc::fa_split_mma_kernel<D>,
+            e = cudaFuncSetAttribute(tc::fa_stream_mma_kernel<D, VI8>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
             if (e != cudaSuccess)
                 return e;
@@ -1249,7 +1651,7 @@ static cudaError_t launch_mma(const Params &p, const CUtensorMap &tmK, const CUt
                 done[dev] = true;
         }
     }
-    tc::fa_split_mma_kernel<D><<<grid, tc::NWARPS * 32, smem, st>>>(p, tmK, tmV);
+    tc::fa_stream_mma_kernel<D, VI8><<<grid, tc::Cfg<D, VI8>::NW * 32, smem, st>>>(p, tmK, tmV);
     return cudaGetLastError();
 }
 
@@ -1312,6 +1714,8 @@ FA_API size_t fa_decode_workspace_size(int batch, int n_q_heads, int n_kv_heads,
 {
     if (batch < 0 || n_q_heads <= 0 || n_kv_heads <= 0 || n_q_heads % n_kv_heads ||
         (head_dim != 128 && head_dim != 256) || max_kv_len < 0)
+        return 0;
+    if (batch == 0)
         return 0;
     if (num_sms <= 0 && device_sms(&num_sms) != 0)
         return 0;
@@ -1381,6 +1785,8 @@ FA_API int fa_decode(const void *q, const void *k_cache, const void *v_cache,
         (paged && overlaps(out, out_bytes, block_table, (size_t)batch * max_blocks_per_seq * 4)) ||
         (window && overlaps(out, out_bytes, window, (size_t)batch * 4)))
         return fail(FA_ERR_ALIAS, "fa_decode: out overlaps an input or the workspace");
+    if (batch == 0)
+        return 0;
     int sms = 0;
     int rc = device_sms(&sms);
     if (rc)
@@ -1410,10 +1816,17 @@ FA_API int fa_decode(const void *q, const void *k_cache, const void *v_cache,
     p.window = window;
     p.out = static_cast<float *>(out);
     p.ws_o = static_cast<float *>(workspace);
-    p.ws_ml = need ? reinterpret_cast<float2 *>(static_cast<char *>(workspace) +
-                                                (size_t)batch * n_q_heads * pl.max_splits * D *
-                                                    sizeof(float))
-                   : nullptr;
+    if (!need) {
+        p.ws_ml = nullptr;
+    } else if (pl.path == Path::Mma) {
+        const size_t slots = (size_t)pl.W + (size_t)batch * pl.units;
+        p.ws_ml = reinterpret_cast<float2 *>(static_cast<char *>(workspace) +
+                                             slots * pl.sh * D * sizeof(float));
+    } else {
+        p.ws_ml = reinterpret_cast<float2 *>(static_cast<char *>(workspace) +
+                                             (size_t)batch * n_q_heads * pl.max_splits * D *
+                                                 sizeof(float));
+    }
     p.B = batch;
     p.Hq = n_q_heads;
     p.Hkv = n_kv_heads;
@@ -1428,9 +1841,13 @@ FA_API int fa_decode(const void *q, const void *k_cache, const void *v_cache,
     p.tile = pl.tile;
     p.tps = pl.tps;
     p.max_splits = pl.max_splits;
+    p.W = pl.W;
+    p.U_b = n_kv_heads * pl.n_hg;
+    p.sh = pl.sh;
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    const dim3 grid(pl.max_splits, n_kv_heads * pl.n_hg, batch);
+    const dim3 grid = pl.path == Path::Mma ? dim3(pl.ctas)
+                                           : dim3(pl.max_splits, n_kv_heads * pl.n_hg, batch);
     cudaEvent_t prof_start = g_prof_start, prof_end = g_prof_end;
     g_prof_start = g_prof_end = nullptr;
     cudaError_t e = cudaSuccess;
@@ -1441,10 +1858,19 @@ FA_API int fa_decode(const void *q, const void *k_cache, const void *v_cache,
     if (e == cudaSuccess && pl.path == Path::Mma) {
         CUtensorMap tmK, tmV;
         const int rk = encode_kv_map(&tmK, k_cache, kv_rows_total, D);
-        const int rv = rk ? rk : encode_kv_map(&tmV, v_cache, kv_rows_total, D);
-        if (rk || rv)
-            return rk ? rk : rv;
-        e = D == 128 ? launch_mma<128>(p, tmK, tmV, grid, st) : launch_mma<256>(p, tmK, tmV, grid, st);
+        if (rk)
+            return rk;
+        if (vi8) {
+            tmV = tmK;   // unused: int8 V arrives by plain bulk copies
+            e = D == 128 ? launch_mma<128, true>(p, tmK, tmV, grid, st)
+                         : launch_mma<256, true>(p, tmK, tmV, grid, st);
+        } else {
+            const int rv = encode_kv_map(&tmV, v_cache, kv_rows_total, D);
+            if (rv)
+                return rv;
+            e = D == 128 ? launch_mma<128, false>(p, tmK, tmV, grid, st)
+                         : launch_mma<256, false>(p, tmK, tmV, grid, st);
+        }
     } else if (e == cudaSuccess) {
         if (D == 128)
             e = vi8 ? dispatch_gp<128, true>(p, pl.gp, grid, st)
@@ -1457,11 +1883,28 @@ FA_API int fa_decode(const void *q, const void *k_cache, const void *v_cache,
         return fail(FA_ERR_CUDA, "fa_decode: split launch failed: %s", cudaGetErrorString(e));
     if (prof_end && (e = cudaEventRecord(prof_end, st)) != cudaSuccess)
         return fail(FA_ERR_CUDA, "fa_decode: profile event: %s", cudaGetErrorString(e));
-    if (D == 128)
-        fa_merge_kernel<128><<<batch * n_q_heads, 32, 0, st>>>(p);
-    else
-        fa_merge_kernel<256><<<batch * n_q_heads, 64, 0, st>>>(p);
-    e = cudaGetLastError();
+    {
+        // programmatic dependent launch: the merge grid is scheduled while the
+        // split grid drains and waits on griddepcontrol.wait for its results
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(batch * n_q_heads);
+        cfg.blockDim = dim3(pl.path == Path::Mma ? tc::MERGE_THREADS : D / 4);
+        cfg.dynamicSmemBytes = 0;
+        cfg.stream = st;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = prof_end ? 0 : 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (pl.path == Path::Mma)
+            e = D == 128 ? cudaLaunchKernelEx(&cfg, tc::fa_stream_merge_kernel<128>, p)
+                         : cudaLaunchKernelEx(&cfg, tc::fa_stream_merge_kernel<256>, p);
+        else
+            e = D == 128 ? cudaLaunchKernelEx(&cfg, fa_merge_kernel<128>, p)
+                         : cudaLaunchKernelEx(&cfg, fa_merge_kernel<256>, p);
+        if (e == cudaSuccess)
+            e = cudaGetLastError();
+    }
     if (e != cudaSuccess)
         return fail(FA_ERR_CUDA, "fa_decode: merge launch failed: %s", cudaGetErrorString(e));
     return 0;

@@ -45,6 +45,13 @@ SMALL = [
     (W("d256_int8_contig", 3, 4, 2, 256, v_int8=True), [3, 200, 511]),
     (W("d128_int8_window", 3, 8, 2, 128, paged=True, v_int8=True, window=100), [50, 500, 333]),
     (W("d128_page64", 3, 8, 2, 128, paged=True, page_size=64), [63, 64, 1000]),
+    # many short ragged sequences (with empty ones): work ranges cross unit
+    # boundaries and units cross work ranges
+    (W("d128_many_ragged", 40, 8, 2, 128, paged=True),
+     [(i * 37) % 211 if i % 7 else 0 for i in range(40)]),
+    (W("d256_many_ragged_int8", 33, 8, 4, 256, paged=True, v_int8=True),
+     [(i * 53) % 301 if i % 5 else 0 for i in range(33)]),
+    (W("d128_g16_long", 2, 32, 2, 128, paged=True), [20000, 9]),
 ]
 
 
