@@ -397,7 +397,9 @@ def run_ours(args, world, rank, local):
                    "head_dim": wl.head_dim, "kv_bytes_per_step": r["kv_bytes"],
                    "l2": r["l2"], "parallelism": f"replicas x{world} (no collectives)"},
         "frac_of_hbm_peak": round(gbs_total / world / peak, 4),
-        "roofline": {"bound": "hbm", "kernel": "fa_split_kernel",
+        "roofline": {"bound": "hbm",
+                     "kernel": ("fa_split_kernel" if os.environ.get("FA_DECODE_KERNEL") == "simt"
+                                else "fa_stream_mma_kernel"),
                      "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                      "peak_kind": peak_kind, "frac": round(achieved / peak, 4),
                      "traffic": None},

@@ -1,29 +1,39 @@
 // fa_decode.cu -- decode-step (single-query) attention over a paged or
 // contiguous KV cache, for sm_103a (GB300).
 //
-// Structure (one launch pair per decode step):
-//   fa_split_kernel  grid (split, kv_head x head_group, sequence).  Each CTA
-//                    owns one split of one sequence's attended key range for
-//                    one KV head and the query heads that share it (GQA).
-//                    NWARPS warps each stream their own tiles (16 tokens at
-//                    head_dim 128, 8 at 256) of K and V into a private ring of
-//                    shared-memory stages with cp.async.bulk (the TMA engine's
-//                    bulk copy) completing on an mbarrier, then run the QK dot,
-//                    the online softmax and the PV accumulate in fp32.  The
-//                    warps' (O, m, l) are merged in shared memory; a sequence
-//                    with one split writes the normalised output directly,
-//                    otherwise the CTA writes an unnormalised partial.
-//   fa_merge_kernel  one CTA per (sequence, query head): log-sum-exp merge of
-//                    the partials, or the zero row of an empty range.
+// One fa_decode call = two launches on the caller's stream:
+//
+//   tc::fa_stream_mma_kernel<D, int8V>   (the default path)
+//       Persistent stream-K kernel.  The step's work is flattened into
+//       16-token tiles ordered by (sequence, KV head [x head group], tile);
+//       each warp of the grid owns an equal contiguous range of that space
+//       and streams it through its own ring of shared-memory stages filled by
+//       TMA (cp.async.bulk.tensor with the 128-byte swizzle for K and fp16 V;
+//       cp.async.bulk for int8 V and its scales).  QK and PV run on the tensor
+//       cores (mma.sync m16n8k16, fp32 accumulate) with the query heads that
+//       share the KV head (up to 8) as the N dimension; the online softmax
+//       sits between them in registers.  At the end of each unit segment the
+//       warp writes the normalised output (it covered the whole unit) or a
+//       partial (O, m, l).
+//   tc::fa_stream_merge_kernel<D>        log-sum-exp merge of the partials,
+//       launched with programmatic dependent launch so it is resident before
+//       the first kernel drains.
+//
+//   fa_split_kernel<D, GP, int8V> + fa_merge_kernel<D>   (FA_DECODE_KERNEL=simt)
+//       The CUDA-core alternative: one CTA per (split, KV head, sequence),
+//       per-warp cp.async.bulk rings, fp32 FMA dots with half-warp transpose
+//       reductions, a shared-memory merge of the warps and a split-count
+//       merge kernel.  Kept for A/B measurement and as an independent second
+//       implementation in the parity tests.
 //
 // The method follows the mlx-native page "flash_attn_vec_hybrid.metal":
-// chunked KV walk with split-K stride, online softmax (running M, S and the
-// rescale of O), the cross-simdgroup merge, and the NWG > 1 partial layout
-// reduced by a separate pass; the tessl page "nn.rs" (flash_attn_decode) for
-// the two-pass FlashDecoding split sized from the fixed capacity, with both
-// passes deriving the same live split count from the device-side length so
-// the scratch needs no zero fill.  Scores are kept in the base-2 domain
-// (scale * log2 e folded into one multiplier), which changes no result.
+// chunked KV walk with split-K, online softmax (running M, S and the rescale
+// of O), the merge of partial (O, S, M) states, and the GQA-grouped variant
+// in which one K/V read serves every query head of its KV head; the tessl page
+// "nn.rs" (flash_attn_decode) for the two-pass FlashDecoding split sized from
+// the fixed capacity, device-side lengths and scratch that needs no zero
+// fill.  Scores are kept in the base-2 domain (scale * log2 e folded into one
+// multiplier), which changes no result.
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -805,6 +815,7 @@ __device__ __forceinline__ long long flat_scan(const Params &p, long long target
 // Workers actually used for T tiles (at least MIN_TPW tiles each), and the
 // worker whose contiguous range holds flattened tile t.
 constexpr int MIN_TPW = 1;
+constexpr int SCAN_REG = 4;     // sequences per lane kept in registers by the one-pass scan
 __device__ __forceinline__ int workers_for(const Params &p, long long T)
 {
     long long w = T / MIN_TPW;
@@ -845,19 +856,65 @@ __global__ void __launch_bounds__(Cfg<D, VI8>::NW * 32, 1)
     const int t4 = lane & 3;         // fragment column pair
     const int w = blockIdx.x * C::NW + warp;
 
-    int b_at;
-    long long P_at;
-    // worker 0 also reports lengths clamped to the capacity
-    const long long T = flat_scan(p, -1, b_at, P_at, w == 0);
-    if (T == 0)
-        return;
-    const int We = workers_for(p, T);
-    if (w >= We)
-        return;
-    const long long t0 = range_start(w, T, We);
-    const long long t1 = range_start(w + 1, T, We);
+    int b_at = -1;
+    long long P_at = 0;
+    long long T, t0, t1;
+    int We;
+    if (p.B <= 32 * SCAN_REG) {
+        // one pass: each lane keeps the tile counts of its sequences
+        // (b = lane + 32 i) in registers, then locates t0 from them
+        long long c[SCAN_REG], x[SCAN_REG], base[SCAN_REG];
+        long long run = 0;
+#pragma unroll
+        for (int i = 0; i < SCAN_REG; ++i) {
+            const int b = lane + 32 * i;
+            c[i] = 0;
+            if (b < p.B) {
+                int lo, hi;
+                attended_range(p, b, lo, hi, w == 0);   // worker 0 reports clamped lengths
+                c[i] = (long long)tiles_in<TILE>(lo, hi) * p.U_b;
+            }
+            x[i] = c[i];
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const long long y = __shfl_up_sync(0xffffffffu, x[i], off);
+                if (lane >= off)
+                    x[i] += y;
+            }
+            base[i] = run;
+            run += __shfl_sync(0xffffffffu, x[i], 31);
+        }
+        T = run;
+        if (T == 0)
+            return;
+        We = workers_for(p, T);
+        if (w >= We)
+            return;
+        t0 = range_start(w, T, We);
+        t1 = range_start(w + 1, T, We);
+#pragma unroll
+        for (int i = 0; i < SCAN_REG; ++i) {
+            const long long excl = base[i] + x[i] - c[i];
+            const unsigned hit =
+                __ballot_sync(0xffffffffu, c[i] > 0 && t0 >= excl && t0 < excl + c[i]);
+            if (hit && b_at < 0) {
+                const int src = __ffs(hit) - 1;
+                b_at = 32 * i + src;
+                P_at = __shfl_sync(0xffffffffu, excl, src);
+            }
+        }
+    } else {
+        T = flat_scan(p, -1, b_at, P_at, w == 0);
+        if (T == 0)
+            return;
+        We = workers_for(p, T);
+        if (w >= We)
+            return;
+        t0 = range_start(w, T, We);
+        t1 = range_start(w + 1, T, We);
+        flat_scan(p, t0, b_at, P_at);
+    }
     const int n_my = static_cast<int>(t1 - t0);
-    flat_scan(p, t0, b_at, P_at);
 
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem = reinterpret_cast<unsigned char *>(
@@ -980,9 +1037,12 @@ __global__ void __launch_bounds__(Cfg<D, VI8>::NW * 32, 1)
                 const uint32_t sc = v8 + C::V8_BYTES;
 #pragma unroll
                 for (int kk = 0; kk < TILE * CPR / 32; ++kk) {
+                    // rows across lanes, chunk index rotated by the row: both
+                    // the int8 reads and the swizzled fp16 writes of each
+                    // 8-lane phase land in 8 different bank groups
                     const int q = lane + 32 * kk;
-                    const int row = q / CPR;
-                    const int cc = q % CPR;
+                    const int row = q % TILE;
+                    const int cc = (q / TILE + row) % CPR;
                     uint32_t o[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
                     if (row >= r0 && row < r1) {
                         uint32_t w0, w1, w2, w3;
