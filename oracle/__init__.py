@@ -17,9 +17,12 @@ C source; in short:
   head_dim elements (dequantisation as ggml ``block_q8_0`` on the
   "dsv4_hc.metal" page; the quantiser rule is the plain symmetric reading);
 * ``gather_rows`` -- bytes of one sequence's cache rows, gathered through the
-  block table.
+  block table;
+* ``append_kv`` -- this step's K / V rows written into the cache at each
+  sequence's position (fp16 rounding, or the int8 codec for V).
 
-Every function here is pinned by ``tests/test_oracle_pins.py``.
+Every function here is pinned by ``tests/test_oracle_pins.py`` and
+``tests/test_oracle_append.py``.
 """
 from __future__ import annotations
 
@@ -69,6 +72,8 @@ def _load():
             lib.oracle_pack_v_int8.restype = i32
             lib.oracle_gather_rows.argtypes = [P, i32, P, i32, i32, i32, i32, i32, P]
             lib.oracle_gather_rows.restype = i32
+            lib.oracle_append_kv.argtypes = [P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32]
+            lib.oracle_append_kv.restype = i32
             lib.oracle_half_to_double.argtypes = [ctypes.c_uint16]
             lib.oracle_half_to_double.restype = dbl
             lib.oracle_double_to_half.argtypes = [dbl]
@@ -200,6 +205,40 @@ def gather_rows(cache, block_table, b, n_tokens, *, n_kv_heads, page_size=16,
     if rc:
         raise OracleError(f"oracle_gather_rows returned {rc}")
     return dense
+
+
+def append_kv(k_new, v_new, k_cache, v_cache, positions, *, v_scales=None, block_table=None,
+              page_size=16, max_blocks=None, num_blocks=None):
+    """Write k_new / v_new ([B, Hkv, D] fp32) into copies of the caches at each
+    sequence's position; returns (k_cache, v_cache, v_scales) as new arrays."""
+    lib = _load()
+    kn = _c(np.asarray(k_new, dtype=np.float32), np.float32)
+    vn = _c(np.asarray(v_new, dtype=np.float32), np.float32)
+    B, Hkv, D = kn.shape
+    kc = np.array(k_cache, copy=True).view(np.uint16)
+    vc = np.array(v_cache, copy=True)
+    if v_scales is None:
+        vc = vc.view(np.uint16)
+        sc = None
+    else:
+        if vc.dtype != np.int8:
+            raise TypeError("int8 V cache expected with v_scales")
+        sc = np.array(v_scales, copy=True).view(np.uint16)
+    pos = _c(np.asarray(positions, dtype=np.int32), np.int32)
+    bt = None if block_table is None else _c(np.asarray(block_table, dtype=np.int32), np.int32)
+    if max_blocks is None:
+        max_blocks = bt.shape[1] if bt is not None else kc.shape[2]
+    if num_blocks is None:
+        num_blocks = kc.shape[0] if bt is not None else 0
+    rc = lib.oracle_append_kv(_ptr(kn), _ptr(vn), _ptr(kc), _ptr(vc), _ptr(sc), _ptr(bt),
+                              _ptr(pos), B, Hkv, D, int(page_size), int(max_blocks),
+                              int(num_blocks))
+    if rc:
+        raise OracleError(f"oracle_append_kv returned {rc}")
+    kc = kc.view(np.float16)
+    if sc is None:
+        return kc, vc.view(np.float16), None
+    return kc, vc, sc.view(np.float16)
 
 
 def half_to_double(bits: int) -> float:

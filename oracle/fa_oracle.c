@@ -24,6 +24,8 @@
  *     workgroup merge reach in exact arithmetic, so the oracle evaluates the
  *     definition instead of that algorithm;
  *   - an empty range gives 0 ("S == 0 ? 0" in the output write).
+ *   The cache append (oracle_append_kv, at the end) writes one step's K and V
+ *   rows at each sequence's position.
  *   The int8 V codec (int8 codes times one fp16 scale per 32 elements) follows
  *   ggml's block_q8_0 dequantisation (qs[i] * d) shown on the DS4Server page
  *   "dsv4_hc.metal"; the quantiser itself (amax / 127, round half to even,
@@ -347,5 +349,59 @@ int oracle_gather_rows(const void *cache, int row_bytes, const int32_t *block_ta
             memcpy(dst + ((long long)kv * n_tokens + t) * row_bytes, src + off,
                    (size_t)row_bytes);
         }
+    return 0;
+}
+
+/*
+ * Cache append: write this step's K and V rows into the cache at each
+ * sequence's device-side position (the per-step "copy K f32 -> f16 into the
+ * cache at cache_pos" of the hf2q page "batched_body.rs", and tessl's
+ * kv_store_timestep on the "nn.rs" page, whose out-of-range offset makes the
+ * store a no-op).
+ *   k_new, v_new: [B][Hkv][D] fp32.
+ *   K row <- fp16 round-to-nearest-even of k_new; V row <- the same for an
+ *   fp16 V cache, or the int8 codec above (codes + per-32 scales).
+ *   A position outside [0, capacity) or a block id outside [0, num_blocks)
+ *   leaves that row untouched.
+ * Returns 0, or a negative code for a bad argument.
+ */
+int oracle_append_kv(const float *k_new, const float *v_new, uint16_t *k_cache, void *v_cache,
+                     uint16_t *v_scales, const int32_t *block_table, const int32_t *positions,
+                     int B, int Hkv, int D, int page_size, int max_blocks, int num_blocks)
+{
+    if (!k_new || !v_new || !k_cache || !v_cache || !positions || B < 0 || Hkv <= 0 || D <= 0)
+        return -1;
+    if (v_scales && D % 32)
+        return -2;
+    if (block_table && page_size <= 0)
+        return -6;
+    long long cap = block_table ? (long long)max_blocks * page_size : (long long)max_blocks;
+    for (int b = 0; b < B; ++b) {
+        long long t = positions[b];
+        if (t < 0 || t >= cap)
+            continue;
+        for (int kv = 0; kv < Hkv; ++kv) {
+            long long row;
+            if (block_table) {
+                long long blk = block_table[(long long)b * max_blocks + t / page_size];
+                if (blk < 0 || blk >= num_blocks)
+                    continue;
+                row = (blk * Hkv + kv) * page_size + t % page_size;
+            } else {
+                row = ((long long)b * Hkv + kv) * max_blocks + t;
+            }
+            const float *kr = k_new + ((long long)b * Hkv + kv) * D;
+            const float *vr = v_new + ((long long)b * Hkv + kv) * D;
+            for (int d = 0; d < D; ++d)
+                k_cache[row * D + d] = oracle_double_to_half((double)kr[d]);
+            if (v_scales) {
+                oracle_pack_v_int8(vr, 1, D, (int8_t *)v_cache + row * D, v_scales + row * (D / 32));
+            } else {
+                uint16_t *vc = (uint16_t *)v_cache;
+                for (int d = 0; d < D; ++d)
+                    vc[row * D + d] = oracle_double_to_half((double)vr[d]);
+            }
+        }
+    }
     return 0;
 }
