@@ -10,9 +10,9 @@ listed under "configs".
 Timing: W untimed warm-up steps, then K timed steps bracketed by a barrier and
 torch.cuda.synchronize() on both sides; each step is timed with CUDA events on
 the launching stream.  When a workload's KV bytes are under 4x the L2 size,
-the steps cycle through enough copies of the inputs that every step reads
-inputs evicted from L2 (more than 4x L2 of other data read since their last
-use); larger workloads read more than L2 per step anyway.  The split kernel's own duration comes from events the library
+L2 is flushed before every step outside its events (512 MiB written, then a
+read-only pass over another 512 MiB so no dirty lines are left to write
+back); larger workloads read more than L2 per step anyway.  The split kernel's own duration comes from events the library
 records around it (fa_decode_profile_next) on the same stream.
 
 --impl reference times the fp64 CPU oracle on the host cores on a bounded
@@ -52,6 +52,27 @@ def parse_args():
     ap.add_argument("--batch", type=int, default=0,
                     help="profiling only: keep the first N sequences of --workload")
     return ap.parse_args()
+
+
+def recorded_traffic(kernel, workload):
+    """DRAM bytes per launch of `kernel` on `workload` from the committed ncu
+    summary, or None when that summary was taken on a different kernel source
+    (the counters then no longer describe the code being timed)."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
+    src = os.path.join(ROOT, "decode_step_kv_gb300", "csrc", "fa_decode.cu")
+    try:
+        text = open(path).read()
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    except OSError:
+        return None
+    recorded_sha = recorded = None
+    for line in text.splitlines():
+        if "source sha256:" in line:
+            recorded_sha = line.split("source sha256:")[1].split()[0].strip()
+        if "traffic_bytes_per_launch:" in line:
+            recorded = int(line.split("traffic_bytes_per_launch:")[1].split()[0])
+    return recorded if recorded_sha == sha else None
 
 
 def measured_peaks():
@@ -188,29 +209,22 @@ def call(wl, d, stream, out=None):
                       stream=stream)
 
 
-INPUT_KEYS = ("q", "k_cache", "v_cache", "v_scales", "block_table", "seq_lens", "window")
+class L2Flush:
+    """Leave L2 holding none of the step's data between timed steps: write a
+    512 MiB buffer (evicts everything) and then reduce over another 512 MiB
+    buffer (a read-only pass, so the lines left in L2 are clean and the timed
+    kernel never pays to write them back).  Runs outside the timed events.
+    Used when a step reads less than 4x L2; larger steps evict L2 by
+    themselves."""
 
+    def __init__(self, device):
+        import torch
+        self.a = torch.empty(512 * 2 ** 20, dtype=torch.uint8, device=device)
+        self.b = torch.zeros(64 * 2 ** 20, dtype=torch.int64, device=device)
 
-def rotation(d, nbytes):
-    """Copies of the step's inputs to cycle through so that each timed step
-    reads inputs that are not in L2: enough copies that the bytes read between
-    two uses of one copy exceed 4x the L2 size.  A single copy when the step's
-    own KV bytes already do."""
-    if nbytes >= 4 * L2_BYTES:
-        return [d], "inputs larger than 4x L2"
-    per_copy = sum(d[k].numel() * d[k].element_size() for k in INPUT_KEYS
-                   if d.get(k) is not None)
-    n = min(4096, max(3, -(-4 * L2_BYTES // nbytes) + 1))
-    n = max(3, min(n, (2 << 30) // max(per_copy, 1)))
-    copies = [d]
-    for _ in range(n - 1):
-        c = dict(d)
-        for k in INPUT_KEYS:
-            if d.get(k) is not None:
-                c[k] = d[k].clone()
-        copies.append(c)
-    return copies, (f"{n} rotating input copies ({n * per_copy / 2**20:.0f} MiB); each step "
-                    f"reads a copy last touched {n - 1} steps earlier (> 4x L2 read since)")
+    def __call__(self, i):
+        self.a.fill_(i & 0xFF)
+        self.b.amax()
 
 
 def time_kernel(wl, d, steps, warmup, world, device, clocks_gpu=None):
@@ -219,11 +233,14 @@ def time_kernel(wl, d, steps, warmup, world, device, clocks_gpu=None):
     from decode_step_kv_gb300 import binding
     from decode_step_kv_gb300.inputs import kv_bytes
     nbytes = kv_bytes(wl, d["lens"], None if d["window"] is None else d["window"].tolist())
-    copies, l2_note = rotation(d, nbytes)
-    R = len(copies)
+    flush = L2Flush(device) if nbytes < 4 * L2_BYTES else None
+    l2_note = ("flushed before every step: 512 MiB written, then 512 MiB read (clean lines)"
+               if flush else "inputs larger than 4x L2")
     stream = torch.cuda.current_stream(device)
     for i in range(warmup):
-        call(wl, copies[i % R], stream)
+        if flush:
+            flush(i)
+        call(wl, d, stream)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(steps)]
     sampler = ClockSampler(clocks_gpu) if clocks_gpu is not None else None
@@ -233,8 +250,10 @@ def time_kernel(wl, d, steps, warmup, world, device, clocks_gpu=None):
         sampler.__enter__()
     t0 = time.perf_counter()
     for i in range(steps):
+        if flush:
+            flush(i)
         ev[i][0].record(stream)
-        call(wl, copies[(warmup + i) % R], stream)
+        call(wl, d, stream)
         ev[i][1].record(stream)
     torch.cuda.synchronize(device)
     wall = time.perf_counter() - t0
@@ -249,13 +268,15 @@ def time_kernel(wl, d, steps, warmup, world, device, clocks_gpu=None):
            for _ in range(steps)]
     torch.cuda.synchronize(device)
     for i in range(steps):
+        if flush:
+            flush(i)
         ev2[i][0].record(stream)
         ev2[i][1].record(stream)   # creates the event; the library re-records it after the split
         binding.fa_decode_profile_next(None, ev2[i][1])
-        call(wl, copies[(warmup + steps + i) % R], stream)
+        call(wl, d, stream)
     torch.cuda.synchronize(device)
     split_ms = [a.elapsed_time(b) for a, b in ev2]
-    del copies
+    del flush
     res = {
         "us_per_step": 1e3 * statistics.mean(step_ms),
         "us_per_step_median": 1e3 * statistics.median(step_ms),
@@ -378,6 +399,9 @@ def run_ours(args, world, rank, local):
     split_us = max_over_ranks(r["split_us"], world)
     gbs_total = world * r["kv_bytes"] / (us * 1e-6) / 1e9
     achieved = r["kv_bytes"] / (split_us * 1e-6) / 1e9
+    kernel = ("fa_split_kernel" if os.environ.get("FA_DECODE_KERNEL") == "simt"
+              else "fa_stream_mma_kernel")
+    traffic = recorded_traffic(kernel, wl.name) if not args.batch else None
     line = {
         "metric": METRIC,
         "value": round(gbs_total, 2),
@@ -397,12 +421,10 @@ def run_ours(args, world, rank, local):
                    "head_dim": wl.head_dim, "kv_bytes_per_step": r["kv_bytes"],
                    "l2": r["l2"], "parallelism": f"replicas x{world} (no collectives)"},
         "frac_of_hbm_peak": round(gbs_total / world / peak, 4),
-        "roofline": {"bound": "hbm",
-                     "kernel": ("fa_split_kernel" if os.environ.get("FA_DECODE_KERNEL") == "simt"
-                                else "fa_stream_mma_kernel"),
+        "roofline": {"bound": "hbm", "kernel": kernel,
                      "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                      "peak_kind": peak_kind, "frac": round(achieved / peak, 4),
-                     "traffic": None},
+                     "traffic": traffic, "algorithmic_bytes": r["kv_bytes"]},
         "gpu_launches": r["launches"],
         "clocks": r.get("clocks"),
     }

@@ -21,6 +21,7 @@ _lib = None
 FA_STATUS_LEN_CLAMPED = 1
 FA_STATUS_BAD_BLOCK = 2
 FA_STATUS_WAIT_TIMEOUT = 4
+FA_STATUS_POS_RANGE = 8
 
 
 class FaDecodeError(RuntimeError):
@@ -48,6 +49,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
             lib.fa_decode_workspace_size.restype = sz
             lib.fa_quantize_v_int8.argtypes = [P, i64, i32, P, P, P]
             lib.fa_quantize_v_int8.restype = i32
+            lib.fa_append_kv.argtypes = [P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, P]
+            lib.fa_append_kv.restype = i32
             lib.fa_gather_kv_debug.argtypes = [P, i32, P, i32, i32, i32, i32, i32, i32, P, P]
             lib.fa_gather_kv_debug.restype = i32
             lib.fa_decode_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint), P]
@@ -140,6 +143,22 @@ def fa_quantize_v_int8(x, codes, scales, *, stream=None):
     D = x.shape[-1]
     rc = load().fa_quantize_v_int8(_ptr(x), x.numel() // D, D, _ptr(codes), _ptr(scales),
                                    _stream(stream))
+    _check(rc)
+
+
+def fa_append_kv(k_new, v_new, k_cache, v_cache, v_scales, block_table, positions, *,
+                 n_kv_heads, head_dim, page_size=16, max_blocks_per_seq=None, num_blocks=None,
+                 stream=None):
+    """Write this step's K / V rows ([B, Hkv, D] fp32) into the cache at `positions`."""
+    batch = k_new.shape[0]
+    if max_blocks_per_seq is None:
+        max_blocks_per_seq = block_table.shape[1] if block_table is not None else k_cache.shape[2]
+    if num_blocks is None:
+        num_blocks = k_cache.shape[0] if block_table is not None else 0
+    rc = load().fa_append_kv(_ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
+                             _ptr(v_scales), _ptr(block_table), _ptr(positions), int(batch),
+                             int(n_kv_heads), int(head_dim), int(page_size),
+                             int(max_blocks_per_seq), int(num_blocks), _stream(stream))
     _check(rc)
 
 

@@ -1304,10 +1304,22 @@ __global__ void __launch_bounds__(MERGE_THREADS) fa_stream_merge_kernel(const Pa
     const long long u = (long long)b * p.U_b + j;
     const int ns = wl - wf + 1;
 
-    // pass 1: global max of the slots' running maxima
+    // (m, l) of the slots: loaded once per thread (one slot per thread per
+    // pass of MERGE_THREADS), reduced to M, turned into weights in shared memory
+    const int c = tid % CH;
+    const int sg = tid / CH;
+    float L = 0.f;
+    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
     float M = -INFINITY;
-    for (int s = tid; s < ns; s += MERGE_THREADS)
-        M = fmaxf(M, p.ws_ml[(wf + s + u) * p.sh + hh].x);
+    float2 mine = make_float2(-INFINITY, 0.f);
+    if (ns <= MERGE_THREADS) {
+        if (tid < ns)
+            mine = p.ws_ml[(wf + tid + u) * p.sh + hh];
+        M = mine.x;
+    } else {
+        for (int s = tid; s < ns; s += MERGE_THREADS)
+            M = fmaxf(M, p.ws_ml[(wf + s + u) * p.sh + hh].x);
+    }
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1)
         M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
@@ -1320,16 +1332,11 @@ __global__ void __launch_bounds__(MERGE_THREADS) fa_stream_merge_kernel(const Pa
         M = fmaxf(M, red[i]);
     __syncthreads();
 
-    float L = 0.f;
-    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-    const int c = tid % CH;
-    const int sg = tid / CH;
     for (int s0 = 0; s0 < ns; s0 += MERGE_MAX_SLOTS) {
         const int cnt = min(MERGE_MAX_SLOTS, ns - s0);
-        // weights of this pass's slots, and their share of the sum
         float Lp = 0.f;
         for (int s = tid; s < cnt; s += MERGE_THREADS) {
-            const float2 v = p.ws_ml[(wf + s0 + s + u) * p.sh + hh];
+            const float2 v = (ns <= MERGE_THREADS) ? mine : p.ws_ml[(wf + s0 + s + u) * p.sh + hh];
             const float a = (v.x == -INFINITY) ? 0.f : ex2(v.x - M);
             wgt[s] = a;
             Lp = fmaf(v.y, a, Lp);
@@ -1419,7 +1426,25 @@ __global__ void __launch_bounds__(D / 4) fa_merge_kernel(const Params p)
 }
 
 // ------------------------------------------------------------ int8 V packer
-// One warp per 32-element block: lane i quantises element i.
+// One 32-element block per warp, lane i holding element i: the block's scale
+// s = fp16_rn(max|x| / 127) (the division in fp64, so the rounding is that of
+// the exact quotient) and code = clamp(rint(x / s), -127, 127), 0 if s == 0.
+__device__ __forceinline__ int8_t quantize32(float xv, __half &scale)
+{
+    float amax = fabsf(xv);
+#pragma unroll
+    for (int m = 16; m >= 1; m >>= 1)
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, m));
+    scale = __double2half(static_cast<double>(amax) / 127.0);
+    const double s = static_cast<double>(__half2float(scale));
+    double qv = 0.0;
+    if (s != 0.0) {
+        qv = rint(static_cast<double>(xv) / s);
+        qv = fmin(fmax(qv, -127.0), 127.0);
+    }
+    return static_cast<int8_t>(qv);
+}
+
 __global__ void fa_quantize_kernel(const float *x, long long n_blocks, int8_t *codes,
                                    __half *scales)
 {
@@ -1427,21 +1452,59 @@ __global__ void fa_quantize_kernel(const float *x, long long n_blocks, int8_t *c
     if (blk >= n_blocks)
         return;
     const int lane = threadIdx.x & 31;
-    const float xv = x[blk * 32 + lane];
-    float amax = fabsf(xv);
-#pragma unroll
-    for (int m = 16; m >= 1; m >>= 1)
-        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, m));
-    const __half sh = __double2half(static_cast<double>(amax) / 127.0);
-    const double s = static_cast<double>(__half2float(sh));
-    double qv = 0.0;
-    if (s != 0.0) {
-        qv = rint(static_cast<double>(xv) / s);
-        qv = fmin(fmax(qv, -127.0), 127.0);
-    }
-    codes[blk * 32 + lane] = static_cast<int8_t>(qv);
+    __half sh;
+    const int8_t c = quantize32(x[blk * 32 + lane], sh);
+    codes[blk * 32 + lane] = c;
     if (lane == 0)
         scales[blk] = sh;
+}
+
+// ------------------------------------------------------------ cache append
+// One CTA per (sequence, KV head): the step's K row (and V row) rounded to
+// fp16, or V packed to int8 codes + per-32 scales, stored at the sequence's
+// device-side position.
+__global__ void fa_append_kernel(const Params p, const float *k_new, const float *v_new,
+                                 __half *k_cache, void *v_cache, __half *v_scales, int D)
+{
+    const int b = blockIdx.x / p.Hkv;
+    const int kv = blockIdx.x % p.Hkv;
+    const long long t = p.seq_lens[b];          // positions
+    if (t < 0 || t >= p.cap) {
+        if (threadIdx.x == 0 && kv == 0)
+            flag(FA_STATUS_POS_RANGE);
+        return;
+    }
+    long long row;
+    if (p.bt) {
+        const long long blk = p.bt[(long long)b * p.max_blocks + t / p.page_size];
+        if (blk < 0 || blk >= p.num_blocks) {
+            if (threadIdx.x == 0)
+                flag(FA_STATUS_BAD_BLOCK);
+            return;
+        }
+        row = (blk * p.Hkv + kv) * p.page_size + t % p.page_size;
+    } else {
+        row = ((long long)b * p.Hkv + kv) * p.cap + t;
+    }
+    const float *kr = k_new + ((long long)b * p.Hkv + kv) * D;
+    const float *vr = v_new + ((long long)b * p.Hkv + kv) * D;
+    for (int d = threadIdx.x; d < D; d += blockDim.x)
+        k_cache[row * D + d] = __float2half_rn(kr[d]);
+    if (!v_scales) {
+        __half *vc = static_cast<__half *>(v_cache);
+        for (int d = threadIdx.x; d < D; d += blockDim.x)
+            vc[row * D + d] = __float2half_rn(vr[d]);
+    } else {
+        int8_t *vc = static_cast<int8_t *>(v_cache);
+        const int lane = threadIdx.x & 31;
+        for (int blk = threadIdx.x >> 5; blk < D / 32; blk += blockDim.x >> 5) {
+            __half sh;
+            const int8_t c = quantize32(vr[blk * 32 + lane], sh);
+            vc[row * D + blk * 32 + lane] = c;
+            if (lane == 0)
+                v_scales[row * (D / 32) + blk] = sh;
+        }
+    }
 }
 
 // ------------------------------------------------------------ gather (debug)
@@ -1991,6 +2054,58 @@ FA_API int fa_quantize_v_int8(const float *x, long long n_rows, int head_dim, in
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess)
         return fail(FA_ERR_CUDA, "fa_quantize_v_int8: launch failed: %s", cudaGetErrorString(e));
+    return 0;
+}
+
+FA_API int fa_append_kv(const float *k_new, const float *v_new, void *k_cache, void *v_cache,
+                        void *v_scales, const int32_t *block_table, const int32_t *positions,
+                        int batch, int n_kv_heads, int head_dim, int page_size,
+                        int max_blocks_per_seq, int num_blocks, void *stream)
+{
+    g_err[0] = 0;
+    if (!k_new || !v_new || !k_cache || !v_cache || !positions)
+        return fail(FA_ERR_NULL, "fa_append_kv: k_new, v_new, caches and positions are required");
+    if (head_dim <= 0 || head_dim % 32)
+        return fail(FA_ERR_HEAD_DIM, "fa_append_kv: head_dim %d must be a positive multiple of 32",
+                    head_dim);
+    if (n_kv_heads <= 0)
+        return fail(FA_ERR_HEADS, "fa_append_kv: n_kv_heads %d", n_kv_heads);
+    const bool paged = block_table != nullptr;
+    if (batch < 0 || max_blocks_per_seq <= 0 ||
+        (paged && (page_size <= 0 || page_size % 16 || num_blocks <= 0)))
+        return fail(FA_ERR_LAYOUT, "fa_append_kv: bad batch, capacity, page size or block count");
+    const long long cap = paged ? (long long)max_blocks_per_seq * page_size
+                                : (long long)max_blocks_per_seq;
+    const size_t new_bytes = (size_t)batch * n_kv_heads * head_dim * sizeof(float);
+    const size_t rows = paged ? (size_t)num_blocks * page_size : (size_t)batch * cap;
+    const size_t kv_rows = rows * n_kv_heads;
+    const void *ins[3] = {k_new, v_new, positions};
+    const size_t in_bytes[3] = {new_bytes, new_bytes, (size_t)batch * 4};
+    for (int i = 0; i < 3; ++i)
+        if (overlaps(k_cache, kv_rows * head_dim * 2, ins[i], in_bytes[i]) ||
+            overlaps(v_cache, kv_rows * head_dim * (v_scales ? 1 : 2), ins[i], in_bytes[i]) ||
+            (v_scales && overlaps(v_scales, kv_rows * (head_dim / 32) * 2, ins[i], in_bytes[i])))
+            return fail(FA_ERR_ALIAS, "fa_append_kv: a cache overlaps k_new, v_new or positions");
+    if ((long long)batch * n_kv_heads > 0x7fffffffll)
+        return fail(FA_ERR_LAYOUT, "fa_append_kv: too many rows");
+    if (batch == 0)
+        return 0;
+    Params p;
+    memset(&p, 0, sizeof(p));
+    p.bt = block_table;
+    p.seq_lens = positions;
+    p.B = batch;
+    p.Hkv = n_kv_heads;
+    p.page_size = paged ? page_size : 16;
+    p.max_blocks = max_blocks_per_seq;
+    p.num_blocks = num_blocks;
+    p.cap = cap;
+    fa_append_kernel<<<batch * n_kv_heads, 128, 0, static_cast<cudaStream_t>(stream)>>>(
+        p, k_new, v_new, static_cast<__half *>(k_cache), v_cache,
+        static_cast<__half *>(v_scales), head_dim);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess)
+        return fail(FA_ERR_CUDA, "fa_append_kv: launch failed: %s", cudaGetErrorString(e));
     return 0;
 }
 

@@ -59,6 +59,7 @@ extern "C" {
 #define FA_STATUS_LEN_CLAMPED 1u   /* a seq_lens entry was < 0 or > capacity and was clamped */
 #define FA_STATUS_BAD_BLOCK 2u     /* a block-table entry was outside [0, num_blocks); tile skipped */
 #define FA_STATUS_WAIT_TIMEOUT 4u  /* a copy wait passed its ~1 s limit; that split's result is void */
+#define FA_STATUS_POS_RANGE 8u     /* fa_append_kv: a position outside [0, capacity); store skipped */
 
 /*
  * fa_decode -- one decode step of attention for `batch` sequences.
@@ -126,6 +127,30 @@ FA_API size_t fa_decode_workspace_size(int batch, int n_q_heads, int n_kv_heads,
  */
 FA_API int fa_quantize_v_int8(const float *x, long long n_rows, int head_dim, int8_t *codes,
                               void *scales, void *stream);
+
+/*
+ * fa_append_kv -- write one decode step's K and V rows into the cache, the
+ * step before attention on every decode (the hf2q page "batched_body.rs"
+ * copies the step's K row f32 -> f16 into the cache at cache_pos; tessl's
+ * kv_store_timestep on the "nn.rs" page stores at a device-side offset and
+ * makes an out-of-range store a no-op).
+ *
+ * k_new, v_new [batch][n_kv_heads][head_dim] fp32 (device).
+ * positions    int32 [batch] (device): the token index t each sequence writes.
+ * For every (b, kv): K row (b, kv, t) <- fp16 round-to-nearest-even of
+ * k_new[b][kv]; V row <- the same for an fp16 V cache (v_scales == NULL), or
+ * the int8 codec of fa_quantize_v_int8 (codes + one fp16 scale per 32).
+ * Cache layouts, block_table, page_size, max_blocks_per_seq and num_blocks
+ * are those of fa_decode.  A position outside [0, capacity) leaves the
+ * sequence's rows untouched and sets FA_STATUS_POS_RANGE; an unmapped block
+ * id (outside [0, num_blocks)) skips that store and sets FA_STATUS_BAD_BLOCK.
+ * head_dim must be a positive multiple of 32.  The caches must not overlap
+ * k_new, v_new or positions.
+ */
+FA_API int fa_append_kv(const float *k_new, const float *v_new, void *k_cache, void *v_cache,
+                        void *v_scales, const int32_t *block_table, const int32_t *positions,
+                        int batch, int n_kv_heads, int head_dim, int page_size,
+                        int max_blocks_per_seq, int num_blocks, void *stream);
 
 /*
  * fa_gather_kv_debug -- copy sequence b's first n_tokens cache rows, through

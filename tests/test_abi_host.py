@@ -105,3 +105,17 @@ def test_quantize_and_gather_reject_bad_arguments(lib):
     assert lib.fa_gather_kv_debug(A, 256, None, 0, 2, 16, 64, 0, 65, A, None) == -6
     assert lib.fa_gather_kv_debug(A, 256, A, 0, 2, 8, 64, 4, 16, A, None) == -6
     assert lib.fa_gather_kv_debug(None, 256, None, 0, 2, 16, 64, 0, 16, A, None) == -1
+
+
+def test_append_rejects_bad_arguments(lib):
+    f = lib.fa_append_kv
+    #        k_new v_new k_cache v_cache scales bt  pos  B  Hkv D   P   maxb nblk stream
+    assert f(None, A, 2 * A, 3 * A, None, None, 4 * A, 1, 2, 128, 16, 64, 0, None) == -1
+    assert f(A, A, 2 * A, 3 * A, None, None, None, 1, 2, 128, 16, 64, 0, None) == -1
+    assert f(A, A, 2 * A, 3 * A, None, None, 4 * A, 1, 2, 100, 16, 64, 0, None) == -2
+    assert f(A, A, 2 * A, 3 * A, None, None, 4 * A, 1, 0, 128, 16, 64, 0, None) == -3
+    assert f(A, A, 2 * A, 3 * A, None, 5 * A, 4 * A, 1, 2, 128, 8, 64, 4, None) == -6
+    assert f(A, A, 2 * A, 3 * A, None, None, 4 * A, 1, 2, 128, 16, 0, 0, None) == -6
+    # the K cache (1 x 2 x 64 x 128 fp16 = 32 KiB from 2A) would overlap k_new at 2A + 4096
+    assert f(2 * A + 4096, A, 2 * A, 3 * A, None, None, 4 * A, 1, 2, 128, 16, 64, 0, None) == -7
+    assert f(A, A, 2 * A, 3 * A, None, None, 4 * A, 0, 2, 128, 16, 64, 0, None) == 0   # no-op
