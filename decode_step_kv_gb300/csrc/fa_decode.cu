@@ -617,12 +617,44 @@ namespace tc {
 constexpr int TILE = 16;
 constexpr int GPH = 8;          // heads per unit (the mma N dimension)
 
+// Build-time tuning (warps per CTA, stages per warp, CTAs per SM); the
+// defaults are the best measured on GB300 across the decode workloads:
+// head_dim 128 takes 2 CTAs x 4 warps x 3 stages (~100 KB each); head_dim 256
+// with fp16 V takes 4 warps x 3 stages of 16 KB; with int8 V the per-tile
+// dequantisation makes more warps worth more than deeper rings (8 x 1).
+#ifndef FA_TC_NW_128
+#define FA_TC_NW_128 4
+#endif
+#ifndef FA_TC_STAGES_128
+#define FA_TC_STAGES_128 3
+#endif
+#ifndef FA_TC_CTAS_128
+#define FA_TC_CTAS_128 2
+#endif
+#ifndef FA_TC_NW_256
+#define FA_TC_NW_256 4
+#endif
+#ifndef FA_TC_STAGES_256
+#define FA_TC_STAGES_256 3
+#endif
+#ifndef FA_TC_CTAS_256
+#define FA_TC_CTAS_256 1
+#endif
+#ifndef FA_TC_NW_256_I8
+#define FA_TC_NW_256_I8 8
+#endif
+#ifndef FA_TC_STAGES_256_I8
+#define FA_TC_STAGES_256_I8 1
+#endif
+#ifndef FA_TC_CTAS_256_I8
+#define FA_TC_CTAS_256_I8 1
+#endif
+
 template <int D, bool VI8>
 struct Cfg {
-    // D=128: 4 warps x 3 stages (~100 KB, two CTAs per SM); D=256: 6 warps x
-    // 2 stages (~200 KB, one CTA per SM) so each scheduler has warps to switch to
-    static constexpr int NW = D == 128 ? 4 : 6;
-    static constexpr int STAGES = D == 128 ? 3 : 2;
+    static constexpr int NW = D == 128 ? FA_TC_NW_128 : (VI8 ? FA_TC_NW_256_I8 : FA_TC_NW_256);
+    static constexpr int STAGES =
+        D == 128 ? FA_TC_STAGES_128 : (VI8 ? FA_TC_STAGES_256_I8 : FA_TC_STAGES_256);
     static constexpr int BOXES = D / 64;                  // 64-column boxes per row
     static constexpr int BOX_BYTES = TILE * 128;          // 16 rows x 128 B
     static constexpr int T_BYTES = BOXES * BOX_BYTES;     // one fp16 tile (K, or fp16 V)
@@ -635,7 +667,8 @@ struct Cfg {
     static constexpr int WARP_BYTES = STAGES * STAGE_BYTES + CVT_BYTES;
     static constexpr int RING_BYTES = NW * WARP_BYTES;
     static constexpr int SMEM = RING_BYTES + NW * STAGES * 8 + 1024;   // + barriers + alignment
-    static constexpr int CTAS_PER_SM = D == 128 ? 2 : 1;
+    static constexpr int CTAS_PER_SM =
+        D == 128 ? FA_TC_CTAS_128 : (VI8 ? FA_TC_CTAS_256_I8 : FA_TC_CTAS_256);
     static_assert(CTAS_PER_SM * (SMEM + 1024) <= 228 * 1024, "shared memory per SM");
 };
 
@@ -814,7 +847,10 @@ __device__ __forceinline__ long long flat_scan(const Params &p, long long target
 
 // Workers actually used for T tiles (at least MIN_TPW tiles each), and the
 // worker whose contiguous range holds flattened tile t.
-constexpr int MIN_TPW = 1;
+#ifndef FA_MIN_TPW
+#define FA_MIN_TPW 1
+#endif
+constexpr int MIN_TPW = FA_MIN_TPW;   // fewest tiles a stream-K worker is given
 constexpr int SCAN_REG = 4;     // sequences per lane kept in registers by the one-pass scan
 __device__ __forceinline__ int workers_for(const Params &p, long long T)
 {
@@ -855,6 +891,13 @@ __global__ void __launch_bounds__(Cfg<D, VI8>::NW * 32, 1)
     const int g4 = lane >> 2;        // fragment row group
     const int t4 = lane & 3;         // fragment column pair
     const int w = blockIdx.x * C::NW + warp;
+    // fetch the TMA descriptors while the lengths are being scanned
+    if (threadIdx.x == 0) {
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmK)) : "memory");
+        if constexpr (!VI8)
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmV))
+                         : "memory");
+    }
 
     int b_at = -1;
     long long P_at = 0;
@@ -1587,7 +1630,8 @@ static Path choose_path(bool vi8)
 // Split planner: sizes splits from batch x kv_heads x capacity so that the
 // grid holds several waves of resident CTAs (the "nwg" of the pages, chosen
 // here from the SM count rather than a fixed bucket).
-static Plan make_plan(Path path, int B, int Hq, int Hkv, int D, long long cap, int num_sms)
+static Plan make_plan(Path path, int B, int Hq, int Hkv, int D, long long cap, int num_sms,
+                      bool vi8)
 {
     Plan pl = {};
     pl.path = path;
@@ -1600,9 +1644,15 @@ static Plan make_plan(Path path, int B, int Hq, int Hkv, int D, long long cap, i
         pl.n_hg = (G + tc::GPH - 1) / tc::GPH;
         pl.sh = G < tc::GPH ? G : tc::GPH;
         pl.units = Hkv * pl.n_hg;
-        const int nw = D == 128 ? tc::Cfg<128, false>::NW : tc::Cfg<256, false>::NW;
-        pl.ctas = (num_sms > 0 ? num_sms : 1) *
-                  (D == 128 ? tc::Cfg<128, false>::CTAS_PER_SM : tc::Cfg<256, false>::CTAS_PER_SM);
+        int nw, cps;
+        if (D == 128) {
+            nw = vi8 ? tc::Cfg<128, true>::NW : tc::Cfg<128, false>::NW;
+            cps = vi8 ? tc::Cfg<128, true>::CTAS_PER_SM : tc::Cfg<128, false>::CTAS_PER_SM;
+        } else {
+            nw = vi8 ? tc::Cfg<256, true>::NW : tc::Cfg<256, false>::NW;
+            cps = vi8 ? tc::Cfg<256, true>::CTAS_PER_SM : tc::Cfg<256, false>::CTAS_PER_SM;
+        }
+        pl.ctas = (num_sms > 0 ? num_sms : 1) * cps;
         pl.W = pl.ctas * nw;
         pl.tps = 0;
         pl.max_splits = 0;
@@ -1844,12 +1894,13 @@ FA_API size_t fa_decode_workspace_size(int batch, int n_q_heads, int n_kv_heads,
         return 0;
     // the caller's V type is not known here: size for whichever kernel needs more
     size_t need = 0;
-    for (Path path : {Path::Simt, Path::Mma}) {
-        const Plan pl = make_plan(path, batch, n_q_heads, n_kv_heads, head_dim, max_kv_len,
-                                  num_sms);
-        const size_t n = plan_workspace(pl, batch, n_q_heads, head_dim);
-        need = n > need ? n : need;
-    }
+    for (Path path : {Path::Simt, Path::Mma})
+        for (bool vi8 : {false, true}) {
+            const Plan pl = make_plan(path, batch, n_q_heads, n_kv_heads, head_dim, max_kv_len,
+                                      num_sms, vi8);
+            const size_t n = plan_workspace(pl, batch, n_q_heads, head_dim);
+            need = n > need ? n : need;
+        }
     return need;
 }
 
@@ -1919,7 +1970,7 @@ FA_API int fa_decode(const void *q, const void *k_cache, const void *v_cache,
                                           : (long long)batch * n_kv_heads * cap;
     if (kv_rows_total >= (1ll << 31))
         path = Path::Simt;   // TMA row coordinates are 32-bit
-    const Plan pl = make_plan(path, batch, n_q_heads, n_kv_heads, D, cap, sms);
+    const Plan pl = make_plan(path, batch, n_q_heads, n_kv_heads, D, cap, sms, vi8);
     const size_t need = plan_workspace(pl, batch, n_q_heads, D);
     if (need > 0 && (!workspace || workspace_bytes < need))
         return fail(FA_ERR_WORKSPACE, "fa_decode: workspace %zu bytes, need %zu", workspace_bytes,

@@ -19,10 +19,12 @@ C source; in short:
 * ``gather_rows`` -- bytes of one sequence's cache rows, gathered through the
   block table;
 * ``append_kv`` -- this step's K / V rows written into the cache at each
-  sequence's position (fp16 rounding, or the int8 codec for V).
+  sequence's position (fp16 rounding, or the int8 codec for V);
+* ``decode_ring`` / ``append_kv_ring`` -- the same over a ring cache (token t
+  at row t % capacity, only the last `capacity` tokens attended).
 
-Every function here is pinned by ``tests/test_oracle_pins.py`` and
-``tests/test_oracle_append.py``.
+Every function here is pinned by ``tests/test_oracle_pins.py``,
+``tests/test_oracle_append.py`` and ``tests/test_oracle_ring.py``.
 """
 from __future__ import annotations
 
@@ -74,6 +76,11 @@ def _load():
             lib.oracle_gather_rows.restype = i32
             lib.oracle_append_kv.argtypes = [P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32]
             lib.oracle_append_kv.restype = i32
+            lib.oracle_fa_decode_ring.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, i32, dbl,
+                                                  P, i32, i32, P]
+            lib.oracle_fa_decode_ring.restype = i32
+            lib.oracle_append_kv_ring.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32]
+            lib.oracle_append_kv_ring.restype = i32
             lib.oracle_half_to_double.argtypes = [ctypes.c_uint16]
             lib.oracle_half_to_double.restype = dbl
             lib.oracle_double_to_half.argtypes = [dbl]
@@ -149,6 +156,58 @@ def decode(q, k_cache, v_cache, seq_lens, *, scale, n_kv_heads, v_scales=None,
     if rc:
         raise OracleError(f"oracle_fa_decode returned {rc}")
     return out.reshape(B, Hq, D) if rows is None else out
+
+
+def decode_ring(q, k_cache, v_cache, seq_lens, *, scale, n_kv_heads, v_scales=None, window=None,
+                rows=None, threads=0):
+    """Oracle output for a ring cache [B, Hkv, capacity, D]: token t at row
+    t % capacity, seq_lens = tokens seen (may exceed capacity)."""
+    lib = _load()
+    qb = _half_bits(q)
+    B, Hq, D = qb.shape
+    kb = _half_bits(k_cache)
+    cap = kb.shape[2]
+    if v_scales is None:
+        vb, sb = _half_bits(v_cache), None
+    else:
+        vb, sb = _c(v_cache, np.int8), _half_bits(v_scales)
+    sl = _c(np.asarray(seq_lens, dtype=np.int32), np.int32)
+    wn = None if window is None else _c(np.asarray(window, dtype=np.int32), np.int32)
+    if rows is None:
+        rr, n = None, B * Hq
+    else:
+        rr = _c(np.asarray(rows, dtype=np.int32), np.int32)
+        n = rr.size
+    out = np.zeros((n, D), dtype=np.float64)
+    rc = lib.oracle_fa_decode_ring(_ptr(qb), _ptr(kb), _ptr(vb), _ptr(sb), _ptr(sl), _ptr(wn), B,
+                                   Hq, int(n_kv_heads), D, int(cap), float(scale), _ptr(rr), n,
+                                   int(threads), _ptr(out))
+    if rc:
+        raise OracleError(f"oracle_fa_decode_ring returned {rc}")
+    return out.reshape(B, Hq, D) if rows is None else out
+
+
+def append_kv_ring(k_new, v_new, k_cache, v_cache, positions, *, v_scales=None):
+    """append_kv for a ring cache: token t goes to row t % capacity."""
+    lib = _load()
+    kn = _c(np.asarray(k_new, dtype=np.float32), np.float32)
+    vn = _c(np.asarray(v_new, dtype=np.float32), np.float32)
+    B, Hkv, D = kn.shape
+    kc = np.array(k_cache, copy=True).view(np.uint16)
+    vc = np.array(v_cache, copy=True)
+    sc = None
+    if v_scales is None:
+        vc = vc.view(np.uint16)
+    else:
+        sc = np.array(v_scales, copy=True).view(np.uint16)
+    pos = _c(np.asarray(positions, dtype=np.int32), np.int32)
+    rc = lib.oracle_append_kv_ring(_ptr(kn), _ptr(vn), _ptr(kc), _ptr(vc), _ptr(sc), _ptr(pos), B,
+                                   Hkv, D, int(kc.shape[2]))
+    if rc:
+        raise OracleError(f"oracle_append_kv_ring returned {rc}")
+    if sc is None:
+        return kc.view(np.float16), vc.view(np.float16), None
+    return kc.view(np.float16), vc, sc.view(np.float16)
 
 
 def weights(q, k_cache, seq_lens, b, h, *, scale, n_kv_heads, block_table=None,

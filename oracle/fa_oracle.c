@@ -136,6 +136,7 @@ typedef struct {
     const int32_t *window;     /* NULL => all global */
     int B, Hq, Hkv, D, page_size, max_blocks;
     double scale;
+    int ring;                  /* contiguous ring cache: token t at row t % capacity */
 } oracle_problem;
 
 /* Element offset of row (b, kv, t) in a cache whose rows hold `row_elems`. */
@@ -147,8 +148,10 @@ static long long row_offset(const oracle_problem *P, int b, int kv, int t,
         int r = t % P->page_size;
         return ((blk * P->Hkv + kv) * P->page_size + r) * (long long)row_elems;
     }
-    /* contiguous: capacity (tokens) = max_blocks */
-    return (((long long)b * P->Hkv + kv) * P->max_blocks + t) * (long long)row_elems;
+    /* contiguous: capacity (tokens) = max_blocks; a ring cache keeps token t
+     * at row t % capacity */
+    long long r = P->ring ? t % P->max_blocks : t;
+    return (((long long)b * P->Hkv + kv) * P->max_blocks + r) * (long long)row_elems;
 }
 
 static double v_elem(const oracle_problem *P, int b, int kv, int t, int d)
@@ -170,6 +173,10 @@ static void attended_range(const oracle_problem *P, int b, int *lo, int *hi)
     int W = P->window ? P->window[b] : 0;
     *hi = L;
     *lo = (W > 0 && L > W) ? L - W : 0;
+    /* a ring cache holds only the last `capacity` tokens (the pages' live
+     * length min(seq_pos + 1, capacity) of the ring storage mode) */
+    if (P->ring && *hi - P->max_blocks > *lo)
+        *lo = *hi - P->max_blocks;
 }
 
 /* Softmax weights p_t, t in [lo, hi), of row (b, h).  p must hold hi-lo. */
@@ -253,8 +260,10 @@ static int validate(const oracle_problem *P)
         return -6;
     long long cap = P->block_table ? (long long)P->max_blocks * P->page_size
                                    : (long long)P->max_blocks;
+    if (P->ring && (P->block_table || P->max_blocks <= 0))
+        return -6;
     for (int b = 0; b < P->B; ++b)
-        if (P->seq_lens[b] < 0 || P->seq_lens[b] > cap)
+        if (P->seq_lens[b] < 0 || (!P->ring && P->seq_lens[b] > cap))
             return -6;
     return 0;
 }
@@ -264,6 +273,9 @@ static int validate(const oracle_problem *P)
  * for all B*Hq rows when rows == NULL.  out: [n_rows][D] double.
  * n_threads <= 0 uses every online core.  Returns 0 or a negative code.
  */
+static int decode_impl(const oracle_problem *Pin, const int32_t *rows, int n_rows, int n_threads,
+                       double *out);
+
 int oracle_fa_decode(const uint16_t *q, const uint16_t *k_cache, const void *v_cache,
                      const uint16_t *v_scales, const int32_t *block_table,
                      const int32_t *seq_lens, const int32_t *window, int B, int Hq,
@@ -271,12 +283,38 @@ int oracle_fa_decode(const uint16_t *q, const uint16_t *k_cache, const void *v_c
                      const int32_t *rows, int n_rows, int n_threads, double *out)
 {
     oracle_problem P = {q, k_cache, v_cache, v_scales, block_table, seq_lens, window,
-                        B, Hq, Hkv, D, page_size, max_blocks, scale};
+                        B, Hq, Hkv, D, page_size, max_blocks, scale, 0};
+    return decode_impl(&P, rows, n_rows, n_threads, out);
+}
+
+/*
+ * Ring cache: contiguous [B][Hkv][capacity][D] storage in which token t of a
+ * sequence lives at row t % capacity; seq_lens counts every token seen (it
+ * may exceed capacity) and only the last `capacity` of them are attended
+ * (the ring storage mode of flash_attn_vec_hybrid_batched on the mlx-native
+ * page: live length min(seq_pos + 1, capacity), rows remapped by ring_start).
+ * The window rule applies on top.
+ */
+int oracle_fa_decode_ring(const uint16_t *q, const uint16_t *k_cache, const void *v_cache,
+                          const uint16_t *v_scales, const int32_t *seq_lens,
+                          const int32_t *window, int B, int Hq, int Hkv, int D, int capacity,
+                          double scale, const int32_t *rows, int n_rows, int n_threads,
+                          double *out)
+{
+    oracle_problem P = {q, k_cache, v_cache, v_scales, NULL, seq_lens, window,
+                        B, Hq, Hkv, D, 1, capacity, scale, 1};
+    return decode_impl(&P, rows, n_rows, n_threads, out);
+}
+
+static int decode_impl(const oracle_problem *Pin, const int32_t *rows, int n_rows, int n_threads,
+                       double *out)
+{
+    oracle_problem P = *Pin;
     int rc = validate(&P);
     if (rc)
         return rc;
     if (!rows)
-        n_rows = B * Hq;
+        n_rows = P.B * P.Hq;
     if (n_threads <= 0)
         n_threads = (int)sysconf(_SC_NPROCESSORS_ONLN);
     if (n_threads > n_rows)
@@ -307,7 +345,7 @@ int oracle_fa_weights(const uint16_t *q, const uint16_t *k_cache,
                       double *p, int *lo_out, int *hi_out)
 {
     oracle_problem P = {q, k_cache, k_cache, NULL, block_table, seq_lens, window,
-                        B, Hq, Hkv, D, page_size, max_blocks, scale};
+                        B, Hq, Hkv, D, page_size, max_blocks, scale, 0};
     int rc = validate(&P);
     if (rc)
         return rc;
@@ -365,9 +403,32 @@ int oracle_gather_rows(const void *cache, int row_bytes, const int32_t *block_ta
  *   leaves that row untouched.
  * Returns 0, or a negative code for a bad argument.
  */
+static int append_impl(const float *k_new, const float *v_new, uint16_t *k_cache, void *v_cache,
+                       uint16_t *v_scales, const int32_t *block_table, const int32_t *positions,
+                       int B, int Hkv, int D, int page_size, int max_blocks, int num_blocks,
+                       int ring);
+
 int oracle_append_kv(const float *k_new, const float *v_new, uint16_t *k_cache, void *v_cache,
                      uint16_t *v_scales, const int32_t *block_table, const int32_t *positions,
                      int B, int Hkv, int D, int page_size, int max_blocks, int num_blocks)
+{
+    return append_impl(k_new, v_new, k_cache, v_cache, v_scales, block_table, positions, B, Hkv,
+                       D, page_size, max_blocks, num_blocks, 0);
+}
+
+/* Append into a ring cache: token t goes to row t % capacity (t >= 0). */
+int oracle_append_kv_ring(const float *k_new, const float *v_new, uint16_t *k_cache,
+                          void *v_cache, uint16_t *v_scales, const int32_t *positions, int B,
+                          int Hkv, int D, int capacity)
+{
+    return append_impl(k_new, v_new, k_cache, v_cache, v_scales, NULL, positions, B, Hkv, D, 1,
+                       capacity, 0, 1);
+}
+
+static int append_impl(const float *k_new, const float *v_new, uint16_t *k_cache, void *v_cache,
+                       uint16_t *v_scales, const int32_t *block_table, const int32_t *positions,
+                       int B, int Hkv, int D, int page_size, int max_blocks, int num_blocks,
+                       int ring)
 {
     if (!k_new || !v_new || !k_cache || !v_cache || !positions || B < 0 || Hkv <= 0 || D <= 0)
         return -1;
@@ -378,8 +439,10 @@ int oracle_append_kv(const float *k_new, const float *v_new, uint16_t *k_cache, 
     long long cap = block_table ? (long long)max_blocks * page_size : (long long)max_blocks;
     for (int b = 0; b < B; ++b) {
         long long t = positions[b];
-        if (t < 0 || t >= cap)
+        if (t < 0 || (!ring && t >= cap))
             continue;
+        if (ring)
+            t %= cap;
         for (int kv = 0; kv < Hkv; ++kv) {
             long long row;
             if (block_table) {
