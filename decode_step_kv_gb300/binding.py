@@ -49,6 +49,11 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
             lib.fa_decode_workspace_size.restype = sz
             lib.fa_quantize_v_int8.argtypes = [P, i64, i32, P, P, P]
             lib.fa_quantize_v_int8.restype = i32
+            lib.fa_decode_ring.argtypes = [P, P, P, P, P, i32, i32, i32, f32, P, P, i32, i32, P,
+                                           sz, P]
+            lib.fa_decode_ring.restype = i32
+            lib.fa_append_kv_ring.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, P]
+            lib.fa_append_kv_ring.restype = i32
             lib.fa_append_kv.argtypes = [P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, P]
             lib.fa_append_kv.restype = i32
             lib.fa_gather_kv_debug.argtypes = [P, i32, P, i32, i32, i32, i32, i32, i32, P, P]
@@ -112,6 +117,27 @@ def fa_decode(q, k_cache, v_cache, v_scales, block_table, seq_lens, n_q_heads, n
                           int(head_dim), float(scale), _ptr(window), _ptr(out), int(batch),
                           int(page_size), int(max_blocks_per_seq), int(num_blocks),
                           _ptr(workspace), ws_bytes, _stream(stream))
+    _check(rc)
+
+
+def fa_decode_ring(q, k_cache, v_cache, v_scales, seq_lens, n_q_heads, n_kv_heads, head_dim,
+                   scale, window, out, *, workspace=None, stream=None):
+    """Decode over a ring cache [B, Hkv, capacity, D]: token t at row t % capacity,
+    seq_lens = tokens seen (may exceed capacity)."""
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = load().fa_decode_ring(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(v_scales),
+                               _ptr(seq_lens), int(n_q_heads), int(n_kv_heads), int(head_dim),
+                               float(scale), _ptr(window), _ptr(out), int(q.shape[0]),
+                               int(k_cache.shape[2]), _ptr(workspace), ws_bytes, _stream(stream))
+    _check(rc)
+
+
+def fa_append_kv_ring(k_new, v_new, k_cache, v_cache, v_scales, positions, *, stream=None):
+    """Write this step's K / V rows into a ring cache at row position % capacity."""
+    rc = load().fa_append_kv_ring(_ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
+                                  _ptr(v_scales), _ptr(positions), int(k_new.shape[0]),
+                                  int(k_new.shape[1]), int(k_new.shape[2]),
+                                  int(k_cache.shape[2]), _stream(stream))
     _check(rc)
 
 

@@ -93,6 +93,7 @@ struct Params {
     int tile;         // tokens per tile
     int tps;          // tiles per split (split kernels)
     int max_splits;
+    int ring;         // contiguous ring cache: token t at row t % cap, lengths unbounded
     int W;            // stream-K workers (warps) in the grid
     int U_b;          // units per sequence: kv heads x head groups
     int sh;           // heads stored per workspace slot (stream-K)
@@ -185,14 +186,17 @@ __device__ __forceinline__ void attended_range(const Params &p, int b, int &lo, 
                                                bool report)
 {
     long long L = p.seq_lens[b];
-    if (L < 0 || L > p.cap) {
+    if (L < 0 || (!p.ring && L > p.cap) || L > 0x7fffffffll) {
         if (report)
             flag(FA_STATUS_LEN_CLAMPED);
-        L = L < 0 ? 0 : p.cap;
+        L = L < 0 ? 0 : (p.ring ? 0x7fffffffll : p.cap);
     }
     const int W = p.window ? p.window[b] : 0;
     hi = static_cast<int>(L);
     lo = (W > 0 && hi > W) ? hi - W : 0;
+    // a ring cache holds only the last cap tokens (live length min(N, cap))
+    if (p.ring && (long long)hi - p.cap > lo)
+        lo = static_cast<int>(hi - p.cap);
 }
 
 template <int TILE>
@@ -212,7 +216,8 @@ __device__ __forceinline__ long long row_offset(const Params &p, int b, int kv, 
             return -1;
         return ((blk * p.Hkv + kv) * p.page_size + tok % p.page_size) * (long long)row_bytes;
     }
-    return (((long long)b * p.Hkv + kv) * p.cap + tok) * (long long)row_bytes;
+    const long long r = p.ring ? tok % p.cap : tok;
+    return (((long long)b * p.Hkv + kv) * p.cap + r) * (long long)row_bytes;
 }
 
 // ------------------------------------------------------------- reductions
@@ -756,7 +761,7 @@ __device__ __forceinline__ long long tile_row(const Params &p, int b, int kv, in
             return -1;
         return (blk * p.Hkv + kv) * p.page_size + tok % p.page_size;
     }
-    return ((long long)b * p.Hkv + kv) * p.cap + tok;
+    return ((long long)b * p.Hkv + kv) * p.cap + (p.ring ? tok % p.cap : tok);
 }
 
 // Per-sequence walk over the flattened tile space.  Units (one KV head and
@@ -1511,7 +1516,9 @@ __global__ void fa_append_kernel(const Params p, const float *k_new, const float
 {
     const int b = blockIdx.x / p.Hkv;
     const int kv = blockIdx.x % p.Hkv;
-    const long long t = p.seq_lens[b];          // positions
+    long long t = p.seq_lens[b];                // positions
+    if (p.ring && t >= 0)
+        t %= p.cap;
     if (t < 0 || t >= p.cap) {
         if (threadIdx.x == 0 && kv == 0)
             flag(FA_STATUS_POS_RANGE);
@@ -1904,12 +1911,46 @@ FA_API size_t fa_decode_workspace_size(int batch, int n_q_heads, int n_kv_heads,
     return need;
 }
 
+static int decode_impl(const void *q, const void *k_cache, const void *v_cache,
+                       const void *v_scales, const int32_t *block_table,
+                       const int32_t *seq_lens, int n_q_heads, int n_kv_heads, int head_dim,
+                       float scale, const int32_t *window, void *out, int batch, int page_size,
+                       int max_blocks_per_seq, int num_blocks, void *workspace,
+                       size_t workspace_bytes, void *stream, bool ring);
+
 FA_API int fa_decode(const void *q, const void *k_cache, const void *v_cache,
                      const void *v_scales, const int32_t *block_table,
                      const int32_t *seq_lens, int n_q_heads, int n_kv_heads, int head_dim,
                      float scale, const int32_t *window, void *out, int batch, int page_size,
                      int max_blocks_per_seq, int num_blocks, void *workspace,
                      size_t workspace_bytes, void *stream)
+{
+    return decode_impl(q, k_cache, v_cache, v_scales, block_table, seq_lens, n_q_heads,
+                       n_kv_heads, head_dim, scale, window, out, batch, page_size,
+                       max_blocks_per_seq, num_blocks, workspace, workspace_bytes, stream, false);
+}
+
+FA_API int fa_decode_ring(const void *q, const void *k_cache, const void *v_cache,
+                          const void *v_scales, const int32_t *seq_lens, int n_q_heads,
+                          int n_kv_heads, int head_dim, float scale, const int32_t *window,
+                          void *out, int batch, int capacity, void *workspace,
+                          size_t workspace_bytes, void *stream)
+{
+    g_err[0] = 0;
+    if (capacity <= 0 || capacity % 16)
+        return fail(FA_ERR_LAYOUT, "fa_decode_ring: capacity %d must be a positive multiple of 16",
+                    capacity);
+    return decode_impl(q, k_cache, v_cache, v_scales, nullptr, seq_lens, n_q_heads, n_kv_heads,
+                       head_dim, scale, window, out, batch, 16, capacity, 0, workspace,
+                       workspace_bytes, stream, true);
+}
+
+static int decode_impl(const void *q, const void *k_cache, const void *v_cache,
+                       const void *v_scales, const int32_t *block_table,
+                       const int32_t *seq_lens, int n_q_heads, int n_kv_heads, int head_dim,
+                       float scale, const int32_t *window, void *out, int batch, int page_size,
+                       int max_blocks_per_seq, int num_blocks, void *workspace,
+                       size_t workspace_bytes, void *stream, bool ring)
 {
     g_err[0] = 0;
     if (!q || !k_cache || !v_cache || !seq_lens || !out)
@@ -1970,7 +2011,9 @@ FA_API int fa_decode(const void *q, const void *k_cache, const void *v_cache,
                                           : (long long)batch * n_kv_heads * cap;
     if (kv_rows_total >= (1ll << 31))
         path = Path::Simt;   // TMA row coordinates are 32-bit
-    const Plan pl = make_plan(path, batch, n_q_heads, n_kv_heads, D, cap, sms, vi8);
+    // a ring's attended range (the last cap tokens) can straddle one more tile
+    const Plan pl = make_plan(path, batch, n_q_heads, n_kv_heads, D, ring ? cap + 16 : cap, sms,
+                              vi8);
     const size_t need = plan_workspace(pl, batch, n_q_heads, D);
     if (need > 0 && (!workspace || workspace_bytes < need))
         return fail(FA_ERR_WORKSPACE, "fa_decode: workspace %zu bytes, need %zu", workspace_bytes,
@@ -2015,6 +2058,7 @@ FA_API int fa_decode(const void *q, const void *k_cache, const void *v_cache,
     p.tile = pl.tile;
     p.tps = pl.tps;
     p.max_splits = pl.max_splits;
+    p.ring = ring ? 1 : 0;
     p.W = pl.W;
     p.U_b = n_kv_heads * pl.n_hg;
     p.sh = pl.sh;
@@ -2157,6 +2201,51 @@ FA_API int fa_append_kv(const float *k_new, const float *v_new, void *k_cache, v
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess)
         return fail(FA_ERR_CUDA, "fa_append_kv: launch failed: %s", cudaGetErrorString(e));
+    return 0;
+}
+
+FA_API int fa_append_kv_ring(const float *k_new, const float *v_new, void *k_cache, void *v_cache,
+                             void *v_scales, const int32_t *positions, int batch, int n_kv_heads,
+                             int head_dim, int capacity, void *stream)
+{
+    g_err[0] = 0;
+    if (!k_new || !v_new || !k_cache || !v_cache || !positions)
+        return fail(FA_ERR_NULL, "fa_append_kv_ring: k_new, v_new, caches and positions are required");
+    if (head_dim <= 0 || head_dim % 32)
+        return fail(FA_ERR_HEAD_DIM, "fa_append_kv_ring: head_dim %d must be a positive multiple of 32",
+                    head_dim);
+    if (n_kv_heads <= 0)
+        return fail(FA_ERR_HEADS, "fa_append_kv_ring: n_kv_heads %d", n_kv_heads);
+    if (batch < 0 || capacity <= 0 || capacity % 16)
+        return fail(FA_ERR_LAYOUT, "fa_append_kv_ring: bad batch or capacity (a multiple of 16)");
+    const size_t new_bytes = (size_t)batch * n_kv_heads * head_dim * sizeof(float);
+    const size_t kv_rows = (size_t)batch * capacity * n_kv_heads;
+    const void *ins[3] = {k_new, v_new, positions};
+    const size_t in_bytes[3] = {new_bytes, new_bytes, (size_t)batch * 4};
+    for (int i = 0; i < 3; ++i)
+        if (overlaps(k_cache, kv_rows * head_dim * 2, ins[i], in_bytes[i]) ||
+            overlaps(v_cache, kv_rows * head_dim * (v_scales ? 1 : 2), ins[i], in_bytes[i]) ||
+            (v_scales && overlaps(v_scales, kv_rows * (head_dim / 32) * 2, ins[i], in_bytes[i])))
+            return fail(FA_ERR_ALIAS, "fa_append_kv_ring: a cache overlaps k_new, v_new or positions");
+    if ((long long)batch * n_kv_heads > 0x7fffffffll)
+        return fail(FA_ERR_LAYOUT, "fa_append_kv_ring: too many rows");
+    if (batch == 0)
+        return 0;
+    Params p;
+    memset(&p, 0, sizeof(p));
+    p.seq_lens = positions;
+    p.B = batch;
+    p.Hkv = n_kv_heads;
+    p.page_size = 16;
+    p.max_blocks = capacity;
+    p.cap = capacity;
+    p.ring = 1;
+    fa_append_kernel<<<batch * n_kv_heads, 128, 0, static_cast<cudaStream_t>(stream)>>>(
+        p, k_new, v_new, static_cast<__half *>(k_cache), v_cache,
+        static_cast<__half *>(v_scales), head_dim);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess)
+        return fail(FA_ERR_CUDA, "fa_append_kv_ring: launch failed: %s", cudaGetErrorString(e));
     return 0;
 }
 

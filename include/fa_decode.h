@@ -104,6 +104,27 @@ FA_API int fa_decode(const void *q, const void *k_cache, const void *v_cache,
                      size_t workspace_bytes, void *stream);
 
 /*
+ * fa_decode_ring -- fa_decode over a ring cache: the storage mode of a
+ * sliding-window layer on the mlx-native page (flash_attn_vec_hybrid_batched,
+ * "sliding ring storage"): each sequence's contiguous [capacity] rows are
+ * reused round-robin, token t living at row t % capacity, and the live
+ * length is min(tokens seen, capacity).
+ *
+ * k_cache, v_cache (and v_scales) [batch][n_kv_heads][capacity][...] as the
+ * contiguous layout of fa_decode; capacity a positive multiple of 16.
+ * seq_lens[b] = tokens sequence b has seen (may exceed capacity); the keys
+ * attended are the last min(seq_lens[b], capacity) tokens, further cut to the
+ * last window[b] when window[b] > 0.  The workspace must hold
+ * fa_decode_workspace_size(batch, n_q_heads, n_kv_heads, head_dim,
+ * capacity + 16, 0) bytes.  Other arguments, rules and errors as fa_decode.
+ */
+FA_API int fa_decode_ring(const void *q, const void *k_cache, const void *v_cache,
+                          const void *v_scales, const int32_t *seq_lens, int n_q_heads,
+                          int n_kv_heads, int head_dim, float scale, const int32_t *window,
+                          void *out, int batch, int capacity, void *workspace,
+                          size_t workspace_bytes, void *stream);
+
+/*
  * fa_decode_workspace_size -- bytes of scratch fa_decode needs for these
  * sizes: the split-K partials (unnormalised O plus running max and sum per
  * query head and split; the "partial scratch B*H*chunks*(D+2)" of tessl's
@@ -151,6 +172,15 @@ FA_API int fa_append_kv(const float *k_new, const float *v_new, void *k_cache, v
                         void *v_scales, const int32_t *block_table, const int32_t *positions,
                         int batch, int n_kv_heads, int head_dim, int page_size,
                         int max_blocks_per_seq, int num_blocks, void *stream);
+
+/*
+ * fa_append_kv_ring -- fa_append_kv into a ring cache of fa_decode_ring:
+ * token positions[b] >= 0 goes to row positions[b] % capacity (a negative
+ * position stores nothing and sets FA_STATUS_POS_RANGE).
+ */
+FA_API int fa_append_kv_ring(const float *k_new, const float *v_new, void *k_cache, void *v_cache,
+                             void *v_scales, const int32_t *positions, int batch, int n_kv_heads,
+                             int head_dim, int capacity, void *stream);
 
 /*
  * fa_gather_kv_debug -- copy sequence b's first n_tokens cache rows, through

@@ -119,3 +119,17 @@ def test_append_rejects_bad_arguments(lib):
     # the K cache (1 x 2 x 64 x 128 fp16 = 32 KiB from 2A) would overlap k_new at 2A + 4096
     assert f(2 * A + 4096, A, 2 * A, 3 * A, None, None, 4 * A, 1, 2, 128, 16, 64, 0, None) == -7
     assert f(A, A, 2 * A, 3 * A, None, None, 4 * A, 0, 2, 128, 16, 64, 0, None) == 0   # no-op
+
+
+def test_ring_rejects_bad_capacity(lib):
+    f = lib.fa_decode_ring
+    #        q  k      v      vs    sl     hq hkv d    scale win  out    B  cap  ws     wsb    st
+    assert f(A, 2 * A, 3 * A, None, 4 * A, 8, 2, 128, 0.1, None, 5 * A, 1, 100, 6 * A, 1 << 30,
+             None) == -6
+    assert f(A, 2 * A, 3 * A, None, 4 * A, 8, 2, 128, 0.1, None, 5 * A, 1, 0, 6 * A, 1 << 30,
+             None) == -6
+    assert f(A, 2 * A, 3 * A, None, None, 8, 2, 128, 0.1, None, 5 * A, 1, 64, 6 * A, 1 << 30,
+             None) == -1
+    g = lib.fa_append_kv_ring
+    assert g(A, A, 2 * A, 3 * A, None, 4 * A, 1, 2, 128, 100, None) == -6
+    assert g(A, A, 2 * A, 3 * A, None, None, 1, 2, 128, 64, None) == -1
