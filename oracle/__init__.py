@@ -20,11 +20,14 @@ C source; in short:
   block table;
 * ``append_kv`` -- this step's K / V rows written into the cache at each
   sequence's position (fp16 rounding, or the int8 codec for V);
+* ``decode_multi`` -- several query tokens per sequence (speculative
+  verify), each attending causally up to its own position;
 * ``decode_ring`` / ``append_kv_ring`` -- the same over a ring cache (token t
   at row t % capacity, only the last `capacity` tokens attended).
 
 Every function here is pinned by ``tests/test_oracle_pins.py``,
-``tests/test_oracle_append.py`` and ``tests/test_oracle_ring.py``.
+``tests/test_oracle_append.py``, ``tests/test_oracle_ring.py`` and
+``tests/test_oracle_multi.py``.
 """
 from __future__ import annotations
 
@@ -79,6 +82,9 @@ def _load():
             lib.oracle_fa_decode_ring.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, i32, dbl,
                                                   P, i32, i32, P]
             lib.oracle_fa_decode_ring.restype = i32
+            lib.oracle_fa_decode_multi.argtypes = [P, P, P, P, P, P, P, i32, i32, i32, i32, i32,
+                                                   i32, i32, dbl, P, i32, i32, P]
+            lib.oracle_fa_decode_multi.restype = i32
             lib.oracle_append_kv_ring.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32]
             lib.oracle_append_kv_ring.restype = i32
             lib.oracle_half_to_double.argtypes = [ctypes.c_uint16]
@@ -156,6 +162,33 @@ def decode(q, k_cache, v_cache, seq_lens, *, scale, n_kv_heads, v_scales=None,
     if rc:
         raise OracleError(f"oracle_fa_decode returned {rc}")
     return out.reshape(B, Hq, D) if rows is None else out
+
+
+def decode_multi(q, k_cache, v_cache, seq_lens, *, scale, n_kv_heads, v_scales=None,
+                 block_table=None, window=None, page_size=16, max_blocks=None, threads=0):
+    """Multi-query decode: q [B, Tq, Hq, D] = each sequence's last Tq tokens;
+    query j attends keys up to its own position.  Returns [B, Tq, Hq, D]."""
+    lib = _load()
+    qb = _half_bits(q)
+    B, Tq, Hq, D = qb.shape
+    kb = _half_bits(k_cache)
+    if v_scales is None:
+        vb, sb = _half_bits(v_cache), None
+    else:
+        vb, sb = _c(v_cache, np.int8), _half_bits(v_scales)
+    sl = _c(np.asarray(seq_lens, dtype=np.int32), np.int32)
+    bt = None if block_table is None else _c(np.asarray(block_table, dtype=np.int32), np.int32)
+    wn = None if window is None else _c(np.asarray(window, dtype=np.int32), np.int32)
+    if max_blocks is None:
+        max_blocks = bt.shape[1] if bt is not None else kb.shape[2]
+    out = np.zeros((B * Tq * Hq, D), dtype=np.float64)
+    rc = lib.oracle_fa_decode_multi(_ptr(qb), _ptr(kb), _ptr(vb), _ptr(sb), _ptr(bt), _ptr(sl),
+                                    _ptr(wn), B, Tq, Hq, int(n_kv_heads), D, int(page_size),
+                                    int(max_blocks), float(scale), None, 0, int(threads),
+                                    _ptr(out))
+    if rc:
+        raise OracleError(f"oracle_fa_decode_multi returned {rc}")
+    return out.reshape(B, Tq, Hq, D)
 
 
 def decode_ring(q, k_cache, v_cache, seq_lens, *, scale, n_kv_heads, v_scales=None, window=None,

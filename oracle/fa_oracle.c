@@ -137,6 +137,7 @@ typedef struct {
     int B, Hq, Hkv, D, page_size, max_blocks;
     double scale;
     int ring;                  /* contiguous ring cache: token t at row t % capacity */
+    int tq;                    /* queries per sequence (q is [B][tq][Hq][D]); 0 or 1 = one */
 } oracle_problem;
 
 /* Element offset of row (b, kv, t) in a cache whose rows hold `row_elems`. */
@@ -167,12 +168,21 @@ static double v_elem(const oracle_problem *P, int b, int kv, int t, int d)
     return code * s;
 }
 
-static void attended_range(const oracle_problem *P, int b, int *lo, int *hi)
+/* Attended keys [lo, hi) of query j of sequence b.  With tq queries the
+ * sequence's last tq tokens are the queries; query j sits at position
+ * L - tq + j and sees the keys up to and including itself (the causal rule
+ * of the tessl page's flash_attn_rows; window 0 = global).  One query: the
+ * whole length. */
+static void attended_range(const oracle_problem *P, int b, int j, int *lo, int *hi)
 {
     int L = P->seq_lens[b];
     int W = P->window ? P->window[b] : 0;
-    *hi = L;
-    *lo = (W > 0 && L > W) ? L - W : 0;
+    int tq = P->tq > 1 ? P->tq : 1;
+    int end = L - (tq - 1 - j);
+    if (end < 0)
+        end = 0;
+    *hi = end;
+    *lo = (W > 0 && end > W) ? end - W : 0;
     /* a ring cache holds only the last `capacity` tokens (the pages' live
      * length min(seq_pos + 1, capacity) of the ring storage mode) */
     if (P->ring && *hi - P->max_blocks > *lo)
@@ -180,11 +190,12 @@ static void attended_range(const oracle_problem *P, int b, int *lo, int *hi)
 }
 
 /* Softmax weights p_t, t in [lo, hi), of row (b, h).  p must hold hi-lo. */
-static void row_weights(const oracle_problem *P, int b, int h, int lo, int hi,
+static void row_weights(const oracle_problem *P, int b, int j, int h, int lo, int hi,
                         double *p)
 {
     int kv = h / (P->Hq / P->Hkv);
-    const uint16_t *qrow = P->q + ((long long)b * P->Hq + h) * P->D;
+    int tq = P->tq > 1 ? P->tq : 1;
+    const uint16_t *qrow = P->q + (((long long)b * tq + j) * P->Hq + h) * P->D;
     double smax = -INFINITY;
     for (int t = lo; t < hi; ++t) {
         const uint16_t *krow = P->k + row_offset(P, b, kv, t, P->D);
@@ -205,17 +216,17 @@ static void row_weights(const oracle_problem *P, int b, int h, int lo, int hi,
         p[t - lo] /= z;
 }
 
-static void row_output(const oracle_problem *P, int b, int h, double *out)
+static void row_output(const oracle_problem *P, int b, int j, int h, double *out)
 {
     int lo, hi;
-    attended_range(P, b, &lo, &hi);
+    attended_range(P, b, j, &lo, &hi);
     for (int d = 0; d < P->D; ++d)
         out[d] = 0.0;
     if (hi <= lo)
         return;
     int kv = h / (P->Hq / P->Hkv);
     double *p = (double *)malloc(sizeof(double) * (size_t)(hi - lo));
-    row_weights(P, b, h, lo, hi, p);
+    row_weights(P, b, j, h, lo, hi, p);
     for (int t = lo; t < hi; ++t)
         for (int d = 0; d < P->D; ++d)
             out[d] += p[t - lo] * v_elem(P, b, kv, t, d);
@@ -242,8 +253,11 @@ static void *worker(void *arg)
         pthread_mutex_unlock(&J->mu);
         if (i >= J->n_rows)
             break;
+        /* row = (b * tq + j) * Hq + h */
         int row = J->rows ? J->rows[i] : i;
-        row_output(J->P, row / J->P->Hq, row % J->P->Hq, J->out + (long long)i * J->P->D);
+        int tq = J->P->tq > 1 ? J->P->tq : 1;
+        int bj = row / J->P->Hq;
+        row_output(J->P, bj / tq, bj % tq, row % J->P->Hq, J->out + (long long)i * J->P->D);
     }
     return NULL;
 }
@@ -283,7 +297,27 @@ int oracle_fa_decode(const uint16_t *q, const uint16_t *k_cache, const void *v_c
                      const int32_t *rows, int n_rows, int n_threads, double *out)
 {
     oracle_problem P = {q, k_cache, v_cache, v_scales, block_table, seq_lens, window,
-                        B, Hq, Hkv, D, page_size, max_blocks, scale, 0};
+                        B, Hq, Hkv, D, page_size, max_blocks, scale, 0, 1};
+    return decode_impl(&P, rows, n_rows, n_threads, out);
+}
+
+/*
+ * Multi-query decode (speculative verify): q [B][tq][Hq][D] holds the last
+ * tq tokens of each sequence, all already in the cache; query j attends the
+ * keys up to its own position L - tq + j (window counted back from there).
+ * out: [B][tq][Hq][D] (or the listed rows, row = (b*tq + j)*Hq + h).
+ * tq = 1 is oracle_fa_decode.
+ */
+int oracle_fa_decode_multi(const uint16_t *q, const uint16_t *k_cache, const void *v_cache,
+                           const uint16_t *v_scales, const int32_t *block_table,
+                           const int32_t *seq_lens, const int32_t *window, int B, int tq, int Hq,
+                           int Hkv, int D, int page_size, int max_blocks, double scale,
+                           const int32_t *rows, int n_rows, int n_threads, double *out)
+{
+    if (tq <= 0)
+        return -6;
+    oracle_problem P = {q, k_cache, v_cache, v_scales, block_table, seq_lens, window,
+                        B, Hq, Hkv, D, page_size, max_blocks, scale, 0, tq};
     return decode_impl(&P, rows, n_rows, n_threads, out);
 }
 
@@ -302,7 +336,7 @@ int oracle_fa_decode_ring(const uint16_t *q, const uint16_t *k_cache, const void
                           double *out)
 {
     oracle_problem P = {q, k_cache, v_cache, v_scales, NULL, seq_lens, window,
-                        B, Hq, Hkv, D, 1, capacity, scale, 1};
+                        B, Hq, Hkv, D, 1, capacity, scale, 1, 1};
     return decode_impl(&P, rows, n_rows, n_threads, out);
 }
 
@@ -314,7 +348,7 @@ static int decode_impl(const oracle_problem *Pin, const int32_t *rows, int n_row
     if (rc)
         return rc;
     if (!rows)
-        n_rows = P.B * P.Hq;
+        n_rows = P.B * (P.tq > 1 ? P.tq : 1) * P.Hq;
     if (n_threads <= 0)
         n_threads = (int)sysconf(_SC_NPROCESSORS_ONLN);
     if (n_threads > n_rows)
@@ -345,16 +379,16 @@ int oracle_fa_weights(const uint16_t *q, const uint16_t *k_cache,
                       double *p, int *lo_out, int *hi_out)
 {
     oracle_problem P = {q, k_cache, k_cache, NULL, block_table, seq_lens, window,
-                        B, Hq, Hkv, D, page_size, max_blocks, scale, 0};
+                        B, Hq, Hkv, D, page_size, max_blocks, scale, 0, 1};
     int rc = validate(&P);
     if (rc)
         return rc;
     int lo, hi;
-    attended_range(&P, b, &lo, &hi);
+    attended_range(&P, b, 0, &lo, &hi);
     *lo_out = lo;
     *hi_out = hi;
     if (hi > lo)
-        row_weights(&P, b, h, lo, hi, p);
+        row_weights(&P, b, 0, h, lo, hi, p);
     return 0;
 }
 
