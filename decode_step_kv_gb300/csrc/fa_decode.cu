@@ -94,6 +94,7 @@ struct Params {
     int tps;          // tiles per split (split kernels)
     int max_splits;
     int ring;         // contiguous ring cache: token t at row t % cap, lengths unbounded
+    int tq;           // queries per sequence (multi-query decode); 1 = one
     int W;            // stream-K workers (warps) in the grid
     int U_b;          // units per sequence: kv heads x head groups
     int sh;           // heads stored per workspace slot (stream-K)
@@ -193,7 +194,10 @@ __device__ __forceinline__ void attended_range(const Params &p, int b, int &lo, 
     }
     const int W = p.window ? p.window[b] : 0;
     hi = static_cast<int>(L);
-    lo = (W > 0 && hi > W) ? hi - W : 0;
+    // with tq queries (the last tq tokens) the window of the first one starts
+    // earliest; each query's own range is masked inside the kernel
+    const int first_end = hi - (p.tq > 1 ? p.tq - 1 : 0);
+    lo = (W > 0 && first_end > W) ? first_end - W : 0;
     // a ring cache holds only the last cap tokens (live length min(N, cap))
     if (p.ring && (long long)hi - p.cap > lo)
         lo = static_cast<int>(hi - p.cap);
@@ -880,6 +884,38 @@ __device__ __forceinline__ int worker_of(long long t, long long T, int We)
 // normalised output (the unit lies wholly in its range) or a partial
 // (O, m, l) to workspace slot w + unit (unique: the workers covering
 // consecutive units are non-decreasing).  The merge kernel folds the slots.
+// Column c (0..7) of column group cg of KV head kv: the (query j, head h)
+// pair x = cg*8 + c = j*G + g (head-fastest); live while x < tq*G.  With one
+// query the columns are the KV head's query heads.
+struct Col {
+    bool live;
+    int j;    // query index within the sequence
+    int h;    // query head
+};
+__device__ __forceinline__ Col column(const Params &p, int kv, int cg, int c)
+{
+    const int tq = p.tq > 1 ? p.tq : 1;
+    const int x = cg * GPH + c;
+    Col r;
+    r.live = x < tq * p.G;
+    r.j = x / p.G;
+    r.h = kv * p.G + x % p.G;
+    return r;
+}
+
+// Keys [lo, hi) column (query j) of sequence b attends: up to and including
+// its own position L - tq + j, the window counted back from there.
+__device__ __forceinline__ void column_range(const Params &p, int b, int L, int j, int &lo,
+                                             int &hi)
+{
+    const int tq = p.tq > 1 ? p.tq : 1;
+    hi = max(L - (tq - 1 - j), 0);
+    const int W = p.window ? p.window[b] : 0;
+    lo = (W > 0 && hi > W) ? hi - W : 0;
+    if (p.ring && (long long)L - p.cap > lo)
+        lo = static_cast<int>(L - p.cap);
+}
+
 template <int D, bool VI8>
 __global__ void __launch_bounds__(Cfg<D, VI8>::NW * 32, 1)
     fa_stream_mma_kernel(const Params p, const __grid_constant__ CUtensorMap tmK,
@@ -1017,34 +1053,40 @@ __global__ void __launch_bounds__(Cfg<D, VI8>::NW * 32, 1)
     }
     __syncwarp();
 
-    // Q^T of the current unit as the QK B operand: b0 = q[head g4][16ks+2t4..], b1 = +8
+    // Q^T of the current unit as the QK B operand: b0 = q[column g4][16ks+2t4..],
+    // b1 = +8; plus this lane's two softmax columns (2t4, 2t4+1) and their key
+    // ranges
+    const int tq = p.tq > 1 ? p.tq : 1;
     uint32_t qb[KS][2];
-    int nh = 0;
+    int nh = 0;                 // live columns of the unit
+    int clo0, chi0, clo1, chi1; // key ranges of columns 2t4 and 2t4+1
     auto load_q = [&](const Walk &u) {
         const int kv = u.j / p.n_hg;
-        const int hg = u.j % p.n_hg;
-        nh = min(GPH, p.G - hg * GPH);
-        const bool live = g4 < nh;
-        const __half *qrow = p.q + ((long long)u.b * p.Hq + kv * p.G + hg * GPH + g4) * D;
+        const int cg = u.j % p.n_hg;
+        nh = min(GPH, tq * p.G - cg * GPH);
+        const Col cq = column(p, kv, cg, g4);
+        const __half *qrow = p.q + (((long long)u.b * tq + cq.j) * p.Hq + cq.h) * D;
 #pragma unroll
         for (int ks = 0; ks < KS; ++ks) {
-            qb[ks][0] = live ? __ldg(reinterpret_cast<const unsigned *>(qrow + ks * 16 + 2 * t4))
-                             : 0u;
-            qb[ks][1] =
-                live ? __ldg(reinterpret_cast<const unsigned *>(qrow + ks * 16 + 8 + 2 * t4)) : 0u;
+            qb[ks][0] = cq.live ? __ldg(reinterpret_cast<const unsigned *>(qrow + ks * 16 + 2 * t4))
+                                : 0u;
+            qb[ks][1] = cq.live
+                            ? __ldg(reinterpret_cast<const unsigned *>(qrow + ks * 16 + 8 + 2 * t4))
+                            : 0u;
         }
+        const Col c0 = column(p, kv, cg, 2 * t4), c1 = column(p, kv, cg, 2 * t4 + 1);
+        column_range(p, u.b, u.hi, c0.live ? c0.j : tq - 1, clo0, chi0);
+        column_range(p, u.b, u.hi, c1.live ? c1.j : tq - 1, clo1, chi1);
     };
     load_q(cw);
     // pull a unit's query rows into L2 when its first tile is issued, so the
-    // switch to that unit does not wait on HBM
+    // switch to that unit does not wait on HBM (lane: column lane/4, line lane%4)
     auto prefetch_q = [&](const Walk &u) {
-        const int kv = u.j / p.n_hg;
-        const int hg = u.j % p.n_hg;
-        const int nq = min(GPH, p.G - hg * GPH);
+        const Col cq = column(p, u.j / p.n_hg, u.j % p.n_hg, lane >> 2);
         const char *base = reinterpret_cast<const char *>(
-            p.q + ((long long)u.b * p.Hq + kv * p.G + hg * GPH) * D);
-        if (lane * 128 < nq * D * 2)
-            asm volatile("prefetch.global.L2 [%0];" ::"l"(base + lane * 128));
+            p.q + (((long long)u.b * tq + cq.j) * p.Hq + cq.h) * D);
+        if (cq.live && (lane & 3) * 128 < D * 2)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(base + (lane & 3) * 128));
     };
 
     float acc[KS][4];
@@ -1152,12 +1194,13 @@ __global__ void __launch_bounds__(Cfg<D, VI8>::NW * 32, 1)
                 for (int r = 0; r < 4; ++r)
                     sc4[r] += sc4b[r];
             }
-            const bool va = g4 >= r0 && g4 < r1;
-            const bool vb = g4 + 8 >= r0 && g4 + 8 < r1;
-            sc4[0] = va ? sc4[0] * p.c2 : -INFINITY;
-            sc4[1] = va ? sc4[1] * p.c2 : -INFINITY;
-            sc4[2] = vb ? sc4[2] * p.c2 : -INFINITY;
-            sc4[3] = vb ? sc4[3] * p.c2 : -INFINITY;
+            // keys outside each column's own range (tile edges, and with
+            // several queries the causal and window limits) weigh nothing
+            const int ka = base + g4, kb = base + g4 + 8;
+            sc4[0] = (ka >= clo0 && ka < chi0) ? sc4[0] * p.c2 : -INFINITY;
+            sc4[1] = (ka >= clo1 && ka < chi1) ? sc4[1] * p.c2 : -INFINITY;
+            sc4[2] = (kb >= clo0 && kb < chi0) ? sc4[2] * p.c2 : -INFINITY;
+            sc4[3] = (kb >= clo1 && kb < chi1) ? sc4[3] * p.c2 : -INFINITY;
             // ---- online softmax per head (lanes sharing t4 share the heads)
             float x0 = fmaxf(sc4[0], sc4[2]);
             float x1 = fmaxf(sc4[1], sc4[3]);
@@ -1168,9 +1211,13 @@ __global__ void __launch_bounds__(Cfg<D, VI8>::NW * 32, 1)
             }
             const float n0 = fmaxf(m0, x0);
             const float n1 = fmaxf(m1, x1);
+            // a column with no key yet keeps max -inf: use 0 as its reference
+            // so every ex2 below sees -inf (weight 0) instead of -inf - -inf
+            const float r0m = n0 == -INFINITY ? 0.f : n0;
+            const float r1m = n1 == -INFINITY ? 0.f : n1;
             if (__any_sync(0xffffffffu, n0 > m0 || n1 > m1)) {
-                const float a0 = ex2(m0 - n0);
-                const float a1 = ex2(m1 - n1);
+                const float a0 = ex2(m0 - r0m);
+                const float a1 = ex2(m1 - r1m);
 #pragma unroll
                 for (int ii = 0; ii < KS; ++ii) {
                     acc[ii][0] *= a0;
@@ -1183,8 +1230,8 @@ __global__ void __launch_bounds__(Cfg<D, VI8>::NW * 32, 1)
                 m0 = n0;
                 m1 = n1;
             }
-            const float p0 = ex2(sc4[0] - m0), p1 = ex2(sc4[1] - m1);
-            const float p2 = ex2(sc4[2] - m0), p3 = ex2(sc4[3] - m1);
+            const float p0 = ex2(sc4[0] - r0m), p1 = ex2(sc4[1] - r1m);
+            const float p2 = ex2(sc4[2] - r0m), p3 = ex2(sc4[3] - r1m);
             l0 += p0 + p2;
             l1 += p1 + p3;
             // ---- P^T as the PV B operand (keys x heads), via movmatrix
@@ -1222,23 +1269,25 @@ __global__ void __launch_bounds__(Cfg<D, VI8>::NW * 32, 1)
             const long long us = cw.unit_start();
             const int wf = worker_of(us, T, We);
             const int wl = worker_of(us + cw.n - 1, T, We);
-            const int hbase = (cw.j / p.n_hg) * p.G + (cw.j % p.n_hg) * GPH;
-            const int h0 = 2 * t4, h1 = 2 * t4 + 1;
+            const int kvu = cw.j / p.n_hg, cgu = cw.j % p.n_hg;
+            const int h0 = 2 * t4, h1 = 2 * t4 + 1;   // this lane's columns
+            const Col c0 = column(p, kvu, cgu, h0), c1 = column(p, kvu, cgu, h1);
             if (wf == wl) {
                 // the whole unit was ours: normalised output
                 const float i0 = l0 > 0.f ? 1.f / l0 : 0.f;
                 const float i1 = l1 > 0.f ? 1.f / l1 : 0.f;
-                float *o = p.out + ((long long)cw.b * p.Hq + hbase) * D;
+                float *o0 = p.out + (((long long)cw.b * tq + c0.j) * p.Hq + c0.h) * D;
+                float *o1 = p.out + (((long long)cw.b * tq + c1.j) * p.Hq + c1.h) * D;
 #pragma unroll
                 for (int mt = 0; mt < KS; ++mt) {
                     const int d = mt * 16 + g4;
-                    if (h0 < nh) {
-                        o[h0 * D + d] = acc[mt][0] * i0;
-                        o[h0 * D + d + 8] = acc[mt][2] * i0;
+                    if (c0.live) {
+                        o0[d] = acc[mt][0] * i0;
+                        o0[d + 8] = acc[mt][2] * i0;
                     }
-                    if (h1 < nh) {
-                        o[h1 * D + d] = acc[mt][1] * i1;
-                        o[h1 * D + d + 8] = acc[mt][3] * i1;
+                    if (c1.live) {
+                        o1[d] = acc[mt][1] * i1;
+                        o1[d + 8] = acc[mt][3] * i1;
                     }
                 }
             } else {
@@ -1296,13 +1345,16 @@ __global__ void __launch_bounds__(MERGE_THREADS) fa_stream_merge_kernel(const Pa
     __shared__ float red[MERGE_THREADS / 32];
     __shared__ float4 part[SG][CH];
 
+    // row = (b * tq + query) * Hq + head; its column x = query * G + head % G
     const long long row = blockIdx.x;
-    const int b = static_cast<int>(row / p.Hq);
+    const int tq = p.tq > 1 ? p.tq : 1;
+    const int b = static_cast<int>(row / ((long long)tq * p.Hq));
+    const int qj = static_cast<int>((row / p.Hq) % tq);
     const int h = static_cast<int>(row % p.Hq);
     const int kv = h / p.G;
-    const int gi = h % p.G;
-    const int j = kv * p.n_hg + gi / GPH;
-    const int hh = gi % GPH;
+    const int x = qj * p.G + h % p.G;
+    const int j = kv * p.n_hg + x / GPH;
+    const int hh = x % GPH;
     const int tid = threadIdx.x;
     const int lane = tid & 31, wid = tid >> 5;
 
@@ -1638,7 +1690,7 @@ static Path choose_path(bool vi8)
 // grid holds several waves of resident CTAs (the "nwg" of the pages, chosen
 // here from the SM count rather than a fixed bucket).
 static Plan make_plan(Path path, int B, int Hq, int Hkv, int D, long long cap, int num_sms,
-                      bool vi8)
+                      bool vi8, int tq = 1)
 {
     Plan pl = {};
     pl.path = path;
@@ -1648,8 +1700,9 @@ static Plan make_plan(Path path, int B, int Hq, int Hkv, int D, long long cap, i
         pl.tile = tc::TILE;
         pl.gp = tc::GPH;
         pl.hpg = tc::GPH;
-        pl.n_hg = (G + tc::GPH - 1) / tc::GPH;
-        pl.sh = G < tc::GPH ? G : tc::GPH;
+        // columns: the (query, head) pairs of one KV head, in groups of 8
+        pl.n_hg = (tq * G + tc::GPH - 1) / tc::GPH;
+        pl.sh = tq * G < tc::GPH ? tq * G : tc::GPH;
         pl.units = Hkv * pl.n_hg;
         int nw, cps;
         if (D == 128) {
@@ -1916,7 +1969,7 @@ static int decode_impl(const void *q, const void *k_cache, const void *v_cache,
                        const int32_t *seq_lens, int n_q_heads, int n_kv_heads, int head_dim,
                        float scale, const int32_t *window, void *out, int batch, int page_size,
                        int max_blocks_per_seq, int num_blocks, void *workspace,
-                       size_t workspace_bytes, void *stream, bool ring);
+                       size_t workspace_bytes, void *stream, bool ring, int tq);
 
 FA_API int fa_decode(const void *q, const void *k_cache, const void *v_cache,
                      const void *v_scales, const int32_t *block_table,
@@ -1927,7 +1980,47 @@ FA_API int fa_decode(const void *q, const void *k_cache, const void *v_cache,
 {
     return decode_impl(q, k_cache, v_cache, v_scales, block_table, seq_lens, n_q_heads,
                        n_kv_heads, head_dim, scale, window, out, batch, page_size,
-                       max_blocks_per_seq, num_blocks, workspace, workspace_bytes, stream, false);
+                       max_blocks_per_seq, num_blocks, workspace, workspace_bytes, stream, false, 1);
+}
+
+FA_API int fa_decode_multi(const void *q, const void *k_cache, const void *v_cache,
+                           const void *v_scales, const int32_t *block_table,
+                           const int32_t *seq_lens, int n_queries, int n_q_heads, int n_kv_heads,
+                           int head_dim, float scale, const int32_t *window, void *out, int batch,
+                           int page_size, int max_blocks_per_seq, int num_blocks,
+                           void *workspace, size_t workspace_bytes, void *stream)
+{
+    g_err[0] = 0;
+    if (n_queries <= 0 || n_queries > 256)
+        return fail(FA_ERR_LAYOUT, "fa_decode_multi: n_queries %d must be in [1, 256]", n_queries);
+    return decode_impl(q, k_cache, v_cache, v_scales, block_table, seq_lens, n_q_heads,
+                       n_kv_heads, head_dim, scale, window, out, batch, page_size,
+                       max_blocks_per_seq, num_blocks, workspace, workspace_bytes, stream, false,
+                       n_queries);
+}
+
+FA_API size_t fa_decode_multi_workspace_size(int batch, int n_queries, int n_q_heads,
+                                             int n_kv_heads, int head_dim, int max_kv_len,
+                                             int num_sms)
+{
+    if (n_queries <= 0 || batch < 0 || n_q_heads <= 0 || n_kv_heads <= 0 ||
+        n_q_heads % n_kv_heads || (head_dim != 128 && head_dim != 256) || max_kv_len < 0)
+        return 0;
+    if (n_queries == 1)
+        return fa_decode_workspace_size(batch, n_q_heads, n_kv_heads, head_dim, max_kv_len,
+                                        num_sms);
+    if (batch == 0)
+        return 0;
+    if (num_sms <= 0 && device_sms(&num_sms) != 0)
+        return 0;
+    size_t need = 0;
+    for (bool vi8 : {false, true}) {
+        const Plan pl = make_plan(Path::Mma, batch, n_q_heads, n_kv_heads, head_dim, max_kv_len,
+                                  num_sms, vi8, n_queries);
+        const size_t n = plan_workspace(pl, batch, n_q_heads, head_dim);
+        need = n > need ? n : need;
+    }
+    return need;
 }
 
 FA_API int fa_decode_ring(const void *q, const void *k_cache, const void *v_cache,
@@ -1942,7 +2035,7 @@ FA_API int fa_decode_ring(const void *q, const void *k_cache, const void *v_cach
                     capacity);
     return decode_impl(q, k_cache, v_cache, v_scales, nullptr, seq_lens, n_q_heads, n_kv_heads,
                        head_dim, scale, window, out, batch, 16, capacity, 0, workspace,
-                       workspace_bytes, stream, true);
+                       workspace_bytes, stream, true, 1);
 }
 
 static int decode_impl(const void *q, const void *k_cache, const void *v_cache,
@@ -1950,7 +2043,7 @@ static int decode_impl(const void *q, const void *k_cache, const void *v_cache,
                        const int32_t *seq_lens, int n_q_heads, int n_kv_heads, int head_dim,
                        float scale, const int32_t *window, void *out, int batch, int page_size,
                        int max_blocks_per_seq, int num_blocks, void *workspace,
-                       size_t workspace_bytes, void *stream, bool ring)
+                       size_t workspace_bytes, void *stream, bool ring, int tq)
 {
     g_err[0] = 0;
     if (!q || !k_cache || !v_cache || !seq_lens || !out)
@@ -1989,10 +2082,10 @@ static int decode_impl(const void *q, const void *k_cache, const void *v_cache,
                                   "must be 16-byte aligned");
     const int D = head_dim;
     // aliasing: out against every input range we can size
-    const size_t out_bytes = (size_t)batch * n_q_heads * D * sizeof(float);
+    const size_t out_bytes = (size_t)batch * tq * n_q_heads * D * sizeof(float);
     const size_t rows = paged ? (size_t)num_blocks * page_size : (size_t)batch * cap;
     const size_t kv_rows = rows * n_kv_heads;
-    if (overlaps(out, out_bytes, q, (size_t)batch * n_q_heads * D * 2) ||
+    if (overlaps(out, out_bytes, q, (size_t)batch * tq * n_q_heads * D * 2) ||
         overlaps(out, out_bytes, k_cache, kv_rows * D * 2) ||
         overlaps(out, out_bytes, v_cache, kv_rows * D * (vi8 ? 1 : 2)) ||
         (vi8 && overlaps(out, out_bytes, v_scales, kv_rows * (D / 32) * 2)) ||
@@ -2009,11 +2102,17 @@ static int decode_impl(const void *q, const void *k_cache, const void *v_cache,
     Path path = choose_path(vi8);
     const long long kv_rows_total = paged ? (long long)num_blocks * n_kv_heads * page_size
                                           : (long long)batch * n_kv_heads * cap;
-    if (kv_rows_total >= (1ll << 31))
+    if (kv_rows_total >= (1ll << 31)) {
+        if (tq > 1)
+            return fail(FA_ERR_LAYOUT, "fa_decode_multi: caches of 2^31 rows or more are not "
+                                       "supported with several queries");
         path = Path::Simt;   // TMA row coordinates are 32-bit
+    }
+    if (tq > 1)
+        path = Path::Mma;    // only the tensor-core kernel has per-column query ranges
     // a ring's attended range (the last cap tokens) can straddle one more tile
     const Plan pl = make_plan(path, batch, n_q_heads, n_kv_heads, D, ring ? cap + 16 : cap, sms,
-                              vi8);
+                              vi8, tq);
     const size_t need = plan_workspace(pl, batch, n_q_heads, D);
     if (need > 0 && (!workspace || workspace_bytes < need))
         return fail(FA_ERR_WORKSPACE, "fa_decode: workspace %zu bytes, need %zu", workspace_bytes,
@@ -2059,6 +2158,7 @@ static int decode_impl(const void *q, const void *k_cache, const void *v_cache,
     p.tps = pl.tps;
     p.max_splits = pl.max_splits;
     p.ring = ring ? 1 : 0;
+    p.tq = tq;
     p.W = pl.W;
     p.U_b = n_kv_heads * pl.n_hg;
     p.sh = pl.sh;
@@ -2105,7 +2205,7 @@ static int decode_impl(const void *q, const void *k_cache, const void *v_cache,
         // programmatic dependent launch: the merge grid is scheduled while the
         // split grid drains and waits on griddepcontrol.wait for its results
         cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(batch * n_q_heads);
+        cfg.gridDim = dim3(batch * tq * n_q_heads);
         cfg.blockDim = dim3(pl.path == Path::Mma ? tc::MERGE_THREADS : D / 4);
         cfg.dynamicSmemBytes = 0;
         cfg.stream = st;

@@ -104,6 +104,33 @@ FA_API int fa_decode(const void *q, const void *k_cache, const void *v_cache,
                      size_t workspace_bytes, void *stream);
 
 /*
+ * fa_decode_multi -- several query tokens per sequence in one call: the
+ * speculative-verify form of the decode step (the n_queries field of the
+ * pages' params; causal rule of tessl's flash_attn_rows on the "nn.rs" page).
+ *
+ * q   [batch][n_queries][n_q_heads][head_dim] fp16: each sequence's last
+ *     n_queries tokens, all already in the cache (seq_lens counts them).
+ * out [batch][n_queries][n_q_heads][head_dim] fp32.
+ * Query j of sequence b sits at position L_b - n_queries + j and attends the
+ * keys up to and including itself; a window W > 0 keeps its last W keys.  A
+ * query whose position is negative gets a zero row.  n_queries = 1 is
+ * fa_decode.  The workspace must hold fa_decode_multi_workspace_size() bytes.
+ * Layouts, other arguments and errors as fa_decode; n_queries in [1, 256].
+ */
+FA_API int fa_decode_multi(const void *q, const void *k_cache, const void *v_cache,
+                           const void *v_scales, const int32_t *block_table,
+                           const int32_t *seq_lens, int n_queries, int n_q_heads, int n_kv_heads,
+                           int head_dim, float scale, const int32_t *window, void *out, int batch,
+                           int page_size, int max_blocks_per_seq, int num_blocks,
+                           void *workspace, size_t workspace_bytes, void *stream);
+
+/* Scratch bytes for fa_decode_multi (host-only; arguments as
+ * fa_decode_workspace_size plus n_queries). */
+FA_API size_t fa_decode_multi_workspace_size(int batch, int n_queries, int n_q_heads,
+                                             int n_kv_heads, int head_dim, int max_kv_len,
+                                             int num_sms);
+
+/*
  * fa_decode_ring -- fa_decode over a ring cache: the storage mode of a
  * sliding-window layer on the mlx-native page (flash_attn_vec_hybrid_batched,
  * "sliding ring storage"): each sequence's contiguous [capacity] rows are

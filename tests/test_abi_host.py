@@ -133,3 +133,15 @@ def test_ring_rejects_bad_capacity(lib):
     g = lib.fa_append_kv_ring
     assert g(A, A, 2 * A, 3 * A, None, 4 * A, 1, 2, 128, 100, None) == -6
     assert g(A, A, 2 * A, 3 * A, None, None, 1, 2, 128, 64, None) == -1
+
+
+def test_multi_rejects_bad_query_count_and_sizes_its_workspace(lib):
+    f = lib.fa_decode_multi
+    args = lambda tq: (A, 2 * A, 3 * A, None, None, 4 * A, tq, 8, 2, 128, 0.1, None, 5 * A, 1,
+                       16, 512, 0, 6 * A, 1 << 30, None)
+    assert f(*args(0)) == -6
+    assert f(*args(257)) == -6
+    g = lib.fa_decode_multi_workspace_size
+    assert g(1, 0, 8, 2, 128, 512, 152) == 0
+    assert g(1, 1, 8, 2, 128, 512, 152) == lib.fa_decode_workspace_size(1, 8, 2, 128, 512, 152)
+    assert g(2, 4, 8, 2, 128, 512, 152) >= g(2, 1, 8, 2, 128, 512, 152)

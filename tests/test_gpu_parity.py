@@ -271,3 +271,28 @@ def test_full_size_workloads_sampled(name):
     assert np.all(np.isfinite(got))
     del dinp
     torch.cuda.empty_cache()
+
+
+def test_many_sequences_take_the_general_length_scan():
+    """More than 128 sequences: the kernels' two-pass scan over the lengths
+    (the one-pass register scan covers up to 128)."""
+    B = 300
+    lens = [(i * 37) % 97 + (0 if i % 11 else 0) for i in range(B)]
+    lens[5] = 0
+    lens[250] = 2000
+    wl = W("many_seqs", B, 8, 2, 128, paged=True, window=50, window_odd_only=True)
+    inp = build_case(wl, seq_lens=lens, spare_blocks=3)
+    want = oracle_decode(wl, inp)
+    got = gpu_decode(wl, to_cuda(inp)).cpu().numpy()
+    assert_close(got, want, False, "300 sequences")
+
+
+def test_one_long_unit_spans_every_worker():
+    """One sequence, one KV head, one query head: the unit's partials come
+    from every worker of the grid, so the merge folds more than 512 slots in
+    several passes."""
+    wl = W("one_unit", 1, 1, 1, 128, paged=True)
+    inp = build_case(wl, seq_lens=[40000])
+    want = oracle_decode(wl, inp)
+    got = gpu_decode(wl, to_cuda(inp)).cpu().numpy()
+    assert_close(got, want, False, "one long unit")
