@@ -67,6 +67,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
             lib.fa_decode_device_status.restype = i32
             lib.fa_decode_profile_next.argtypes = [P, P]
             lib.fa_decode_profile_next.restype = i32
+            lib.fa_selftest_wait_timeout.argtypes = [P]
+            lib.fa_selftest_wait_timeout.restype = i32
             lib.fa_decode_last_error.argtypes = []
             lib.fa_decode_last_error.restype = ctypes.c_char_p
             _lib = lib
@@ -237,6 +239,11 @@ def fa_decode_profile_next(split_start=None, split_end=None):
     if (split_start is not None and not a.value) or (split_end is not None and not b.value):
         raise ValueError("fa_decode_profile_next: event not created yet (record it once first)")
     _check(load().fa_decode_profile_next(a, b))
+
+
+def fa_selftest_wait_timeout(*, stream=None):
+    """Launch the bounded-wait self-test (about one second; sets FA_STATUS_WAIT_TIMEOUT)."""
+    _check(load().fa_selftest_wait_timeout(_stream(stream)))
 
 
 def fa_decode_device_status(*, stream=None) -> int:

@@ -1609,6 +1609,22 @@ __global__ void fa_append_kernel(const Params p, const float *k_new, const float
     }
 }
 
+// ------------------------------------------------------------ wait self-test
+// Arms a barrier that nothing will complete and waits on it with the bounded
+// wait the decode kernels use: after ~1 s the wait gives up and the status
+// bit is set, exactly as a copy that never lands would be reported.
+__global__ void fa_wait_selftest_kernel()
+{
+    __shared__ __align__(8) uint64_t bar;
+    const uint32_t a = smem_u32(&bar);
+    if (threadIdx.x == 0)
+        mbar_init(a, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    __syncwarp();
+    if (!mbar_wait_warp(a, 0) && threadIdx.x == 0)
+        flag(FA_STATUS_WAIT_TIMEOUT);
+}
+
 // ------------------------------------------------------------ gather (debug)
 __global__ void fa_gather_kernel(const Params p, int row_bytes, int b, int n_tokens,
                                  unsigned char *dense)
@@ -2424,6 +2440,17 @@ FA_API int fa_decode_profile_next(void *split_start, void *split_end)
     g_err[0] = 0;
     g_prof_start = static_cast<cudaEvent_t>(split_start);
     g_prof_end = static_cast<cudaEvent_t>(split_end);
+    return 0;
+}
+
+FA_API int fa_selftest_wait_timeout(void *stream)
+{
+    g_err[0] = 0;
+    fa_wait_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>();
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess)
+        return fail(FA_ERR_CUDA, "fa_selftest_wait_timeout: launch failed: %s",
+                    cudaGetErrorString(e));
     return 0;
 }
 

@@ -224,6 +224,17 @@ FA_API int fa_gather_kv_debug(const void *cache, int row_bytes, const int32_t *b
                               int num_blocks, int n_tokens, void *dense, void *stream);
 
 /*
+ * fa_selftest_wait_timeout -- failure-path self-test (no counterpart on the
+ * pages).  Launches one warp that arms a shared-memory barrier nothing will
+ * complete and waits on it with the same bounded wait the decode kernels use
+ * for their copies.  After about one second the wait gives up, the warp exits
+ * and FA_STATUS_WAIT_TIMEOUT is set, showing that a copy that never lands
+ * surfaces as a status bit (read with fa_decode_device_status) rather than a
+ * hang, with the context still usable.
+ */
+FA_API int fa_selftest_wait_timeout(void *stream);
+
+/*
  * fa_decode_device_status -- wait for `stream`, then read and clear the
  * device-side FA_STATUS_* bits accumulated since the last call.
  */

@@ -52,6 +52,10 @@ SMALL = [
     (W("d256_many_ragged_int8", 33, 8, 4, 256, paged=True, v_int8=True),
      [(i * 53) % 301 if i % 5 else 0 for i in range(33)]),
     (W("d128_g16_long", 2, 32, 2, 128, paged=True), [20000, 9]),
+    # the largest GQA group accepted (64 query heads on one KV head) and the
+    # narrowest window (only the newest token)
+    (W("d128_g64", 2, 64, 1, 128, paged=True), [3000, 77]),
+    (W("d256_window1", 3, 4, 2, 256, paged=True, window=1), [1, 2, 999]),
 ]
 
 
