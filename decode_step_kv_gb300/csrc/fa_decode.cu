@@ -630,7 +630,8 @@ constexpr int GPH = 8;          // heads per unit (the mma N dimension)
 // defaults are the best measured on GB300 across the decode workloads:
 // head_dim 128 takes 2 CTAs x 4 warps x 3 stages (~100 KB each); head_dim 256
 // with fp16 V takes 4 warps x 3 stages of 16 KB; with int8 V the per-tile
-// dequantisation makes more warps worth more than deeper rings (8 x 1).
+// dequantisation wants warps to switch between, so V is dequantised in place
+// over the consumed K tile and the freed memory buys 8 warps x 2 stages.
 #ifndef FA_TC_NW_128
 #define FA_TC_NW_128 4
 #endif
@@ -653,10 +654,15 @@ constexpr int GPH = 8;          // heads per unit (the mma N dimension)
 #define FA_TC_NW_256_I8 8
 #endif
 #ifndef FA_TC_STAGES_256_I8
-#define FA_TC_STAGES_256_I8 1
+#define FA_TC_STAGES_256_I8 2
 #endif
 #ifndef FA_TC_CTAS_256_I8
 #define FA_TC_CTAS_256_I8 1
+#endif
+// int8 V: dequantise into the stage's K region once QK has consumed it (1),
+// or into a separate per-warp tile (0)
+#ifndef FA_I8_INPLACE
+#define FA_I8_INPLACE 1
 #endif
 
 template <int D, bool VI8>
@@ -672,7 +678,7 @@ struct Cfg {
     static constexpr int V_STAGE = VI8 ? V8_BYTES + S_BYTES : T_BYTES;
     static constexpr int TX_BYTES = T_BYTES + V_STAGE;    // bytes landing per stage
     static constexpr int STAGE_BYTES = (TX_BYTES + 1023) / 1024 * 1024;
-    static constexpr int CVT_BYTES = VI8 ? T_BYTES : 0;   // per-warp dequantised V tile
+    static constexpr int CVT_BYTES = (VI8 && !FA_I8_INPLACE) ? T_BYTES : 0;   // dequantised V
     static constexpr int WARP_BYTES = STAGES * STAGE_BYTES + CVT_BYTES;
     static constexpr int RING_BYTES = NW * WARP_BYTES;
     static constexpr int SMEM = RING_BYTES + NW * STAGES * 8 + 1024;   // + barriers + alignment
@@ -1115,13 +1121,11 @@ __global__ void __launch_bounds__(Cfg<D, VI8>::NW * 32, 1)
         const int r1 = min(cw.hi - base, TILE);
         const bool block_ok = tile_row(p, cw.b, kv, base) >= 0;
         const uint32_t sK = ring + s * C::STAGE_BYTES;
-        const uint32_t sV = VI8 ? cvt : sK + C::T_BYTES;
+        const uint32_t sV = VI8 ? (FA_I8_INPLACE ? sK : cvt) : sK + C::T_BYTES;
 
-        if (block_ok) {
-            if constexpr (VI8) {
-                // dequantise the int8 tile into the warp's fp16 tile (same
-                // swizzled layout as a TMA-loaded one); keys outside [r0, r1)
-                // become zero rows
+        // int8 V: dequantise the tile into an fp16 tile at sV (same swizzled
+        // layout as a TMA-loaded one); keys outside [r0, r1) become zero rows
+        auto dequant_v = [&] {
                 constexpr int CPR = D / 16;               // 16-code chunks per row
                 const uint32_t v8 = sK + C::T_BYTES;
                 const uint32_t sc = v8 + C::V8_BYTES;
@@ -1150,15 +1154,21 @@ __global__ void __launch_bounds__(Cfg<D, VI8>::NW * 32, 1)
                         dequant4(w3, s2, o[6], o[7]);
                     }
                     asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(
-                                     swz(cvt, row, 2 * cc)),
+                                     swz(sV, row, 2 * cc)),
                                  "r"(o[0]), "r"(o[1]), "r"(o[2]), "r"(o[3])
                                  : "memory");
                     asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(
-                                     swz(cvt, row, 2 * cc + 1)),
+                                     swz(sV, row, 2 * cc + 1)),
                                  "r"(o[4]), "r"(o[5]), "r"(o[6]), "r"(o[7])
                                  : "memory");
                 }
                 __syncwarp();
+        };
+
+        if (block_ok) {
+            if constexpr (VI8) {
+                if constexpr (!FA_I8_INPLACE)
+                    dequant_v();
             } else if (r0 != 0 || r1 != TILE) {
                 // keys outside [r0, r1) hold other tokens' data: zero their V
                 // rows (a 128-byte row segment per box) so 0-weights stay 0
@@ -1193,6 +1203,10 @@ __global__ void __launch_bounds__(Cfg<D, VI8>::NW * 32, 1)
 #pragma unroll
                 for (int r = 0; r < 4; ++r)
                     sc4[r] += sc4b[r];
+            }
+            if constexpr (VI8 && FA_I8_INPLACE) {
+                __syncwarp();        // every lane's K reads are done: reuse the region
+                dequant_v();
             }
             // keys outside each column's own range (tile edges, and with
             // several queries the causal and window limits) weigh nothing
@@ -1249,6 +1263,8 @@ __global__ void __launch_bounds__(Cfg<D, VI8>::NW * 32, 1)
                 }
             }
         }
+        if constexpr (VI8 && FA_I8_INPLACE)
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // before TMA refills it
         __syncwarp();
         if (i + STAGES < n_my) {
             if (pw.k == 0)
