@@ -611,12 +611,14 @@ __global__ void __launch_bounds__(THREADS, 2) fa_split_kernel(const Params p)
 }
 
 // ------------------------------------------------------ tensor-core split kernel
-// Same split / merge contract as fa_split_kernel, with the two contractions on
-// the tensor cores.  Per 16-key tile and per warp:
-//   S[16 keys x 8 heads]   = K_tile[16 x D] . Q^T[D x 8]       (D/16 mma.m16n8k16)
-//   O^T[D x 8 heads]      += V_tile^T[D x 16] . P^T[16 x 8]     (D/16 mma.m16n8k16)
-// The query heads of one KV head sit on the N = 8 dimension (a group of up to
-// 8 heads is one dense column block; larger groups split into head groups).
+// The same (O, m, l) partial and log-sum-exp contract as fa_split_kernel, with
+// stream-K work ranges and the two contractions on the tensor cores.  Per
+// 16-key tile and per warp:
+//   S[16 keys x 8 columns]   = K_tile[16 x D] . Q^T[D x 8]     (D/16 mma.m16n8k16)
+//   O^T[D x 8 columns]      += V_tile^T[D x 16] . P^T[16 x 8]   (D/16 mma.m16n8k16)
+// The N = 8 columns are the query heads that share the KV head (with several
+// queries per sequence: the (query, head) pairs); more than 8 columns split
+// into column groups, each its own unit.
 // K and V tiles arrive by TMA tiled copies (cp.async.bulk.tensor, 64-column
 // boxes, 128-byte swizzle), so the ldmatrix row reads are bank-conflict-free.
 // P is rounded to fp16 for the PV product (accumulation stays fp32); its
@@ -1709,9 +1711,8 @@ static int next_pow2(int x)
 // FA_DECODE_KERNEL=simt selects the CUDA-core one (for A/B measurements; both
 // compute the same result within the tolerances) or the cache is too large
 // for 32-bit TMA row coordinates.
-static Path choose_path(bool vi8)
+static Path choose_path()
 {
-    (void)vi8;
     const char *e = getenv("FA_DECODE_KERNEL");
     if (e && !strcmp(e, "simt"))
         return Path::Simt;
@@ -2131,7 +2132,7 @@ static int decode_impl(const void *q, const void *k_cache, const void *v_cache,
     int rc = device_sms(&sms);
     if (rc)
         return rc;
-    Path path = choose_path(vi8);
+    Path path = choose_path();
     const long long kv_rows_total = paged ? (long long)num_blocks * n_kv_heads * page_size
                                           : (long long)batch * n_kv_heads * cap;
     if (kv_rows_total >= (1ll << 31)) {
