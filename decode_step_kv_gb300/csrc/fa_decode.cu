@@ -98,6 +98,8 @@ struct Params {
     int W;            // stream-K workers (warps) in the grid
     int U_b;          // units per sequence: kv heads x head groups
     int sh;           // heads stored per workspace slot (stream-K)
+    long long *pref;  // stream-K, more than 32*SCAN_REG sequences: [B+1] flattened
+                      // start tile of each sequence (last entry: all tiles)
 };
 
 // ------------------------------------------------------------ PTX wrappers
@@ -826,7 +828,8 @@ struct Walk {
 // target >= 0 also the sequence holding flattened tile `target` and that
 // sequence's first flattened tile.  Every lane returns the same values.
 __device__ __forceinline__ long long flat_scan(const Params &p, long long target, int &b_at,
-                                               long long &P_at, bool report = false)
+                                               long long &P_at, bool report = false,
+                                               long long *pref = nullptr)
 {
     const int lane = threadIdx.x & 31;
     long long run = 0;
@@ -848,6 +851,8 @@ __device__ __forceinline__ long long flat_scan(const Params &p, long long target
                 x += y;
         }
         const long long excl = run + x - c;
+        if (pref && b < p.B)
+            pref[b] = excl;
         if (target >= 0 && b_at < 0) {
             const unsigned hit = __ballot_sync(0xffffffffu, b < p.B && target >= excl &&
                                                                 target < excl + c);
@@ -859,6 +864,8 @@ __device__ __forceinline__ long long flat_scan(const Params &p, long long target
         }
         run += __shfl_sync(0xffffffffu, x, 31);
     }
+    if (pref && lane == 0)
+        pref[p.B] = run;
     return run;
 }
 
@@ -957,10 +964,15 @@ __global__ void __launch_bounds__(Cfg<D, VI8>::NW * 32, 1)
         // (b = lane + 32 i) in registers, then locates t0 from them
         long long c[SCAN_REG], x[SCAN_REG], base[SCAN_REG];
         long long run = 0;
+        const int nblk = (p.B + 31) / 32;       // blocks of 32 sequences in use
 #pragma unroll
         for (int i = 0; i < SCAN_REG; ++i) {
             const int b = lane + 32 * i;
             c[i] = 0;
+            x[i] = 0;
+            base[i] = run;
+            if (i >= nblk)                       // warp-uniform: nothing left to scan
+                continue;
             if (b < p.B) {
                 int lo, hi;
                 attended_range(p, b, lo, hi, w == 0);   // worker 0 reports clamped lengths
@@ -973,7 +985,6 @@ __global__ void __launch_bounds__(Cfg<D, VI8>::NW * 32, 1)
                 if (lane >= off)
                     x[i] += y;
             }
-            base[i] = run;
             run += __shfl_sync(0xffffffffu, x[i], 31);
         }
         T = run;
@@ -986,17 +997,20 @@ __global__ void __launch_bounds__(Cfg<D, VI8>::NW * 32, 1)
         t1 = range_start(w + 1, T, We);
 #pragma unroll
         for (int i = 0; i < SCAN_REG; ++i) {
+            if (i >= nblk || b_at >= 0)
+                continue;
             const long long excl = base[i] + x[i] - c[i];
             const unsigned hit =
                 __ballot_sync(0xffffffffu, c[i] > 0 && t0 >= excl && t0 < excl + c[i]);
-            if (hit && b_at < 0) {
+            if (hit) {
                 const int src = __ffs(hit) - 1;
                 b_at = 32 * i + src;
                 P_at = __shfl_sync(0xffffffffu, excl, src);
             }
         }
     } else {
-        T = flat_scan(p, -1, b_at, P_at, w == 0);
+        // worker 0 also publishes each sequence's flattened start for the merge
+        T = flat_scan(p, -1, b_at, P_at, w == 0, w == 0 ? p.pref : nullptr);
         if (T == 0)
             return;
         We = workers_for(p, T);
@@ -1384,10 +1398,12 @@ __global__ void __launch_bounds__(MERGE_THREADS) fa_stream_merge_kernel(const Pa
             reinterpret_cast<float4 *>(p.out + row * D)[tid] = make_float4(0.f, 0.f, 0.f, 0.f);
         return;
     }
-    // T and the flattened start of sequence b (warp 0 scans; all warps then
-    // read the results from shared memory)
+    // T and the flattened start of sequence b: scanned here for up to
+    // 32*SCAN_REG sequences (before the dependency wait, so it overlaps the
+    // split kernel's tail), else published by the split kernel's worker 0
     __shared__ long long sh_T, sh_P;
-    if (wid == 0) {
+    const bool scan_here = p.B <= 32 * SCAN_REG;
+    if (scan_here && wid == 0) {
         int b_at;
         long long P_at;
         const long long T = flat_scan(p, -1, b_at, P_at);
@@ -1410,6 +1426,13 @@ __global__ void __launch_bounds__(MERGE_THREADS) fa_stream_merge_kernel(const Pa
             sh_P = run;
         }
     }
+    if (!scan_here) {
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        if (tid == 0) {
+            sh_T = p.pref[p.B];
+            sh_P = p.pref[b];
+        }
+    }
     __syncthreads();
     const long long T = sh_T;
     const int We = workers_for(p, T);
@@ -1418,7 +1441,8 @@ __global__ void __launch_bounds__(MERGE_THREADS) fa_stream_merge_kernel(const Pa
     const int wl = worker_of(us + n - 1, T, We);
     if (wf == wl)
         return;                                   // written by the split kernel
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (scan_here)
+        asm volatile("griddepcontrol.wait;" ::: "memory");
     const long long u = (long long)b * p.U_b + j;
     const int ns = wl - wf + 1;
 
@@ -1783,7 +1807,9 @@ static size_t plan_workspace(const Plan &pl, int B, int Hq, int D)
         // partial slots: one per (worker, unit) pair, at most W + units
         (void)Hq;
         const size_t slots = (size_t)pl.W + (size_t)B * pl.units;
-        return slots * pl.sh * (D * sizeof(float) + sizeof(float2));
+        // + the per-sequence prefix published for batches the merge does not scan
+        return slots * pl.sh * (D * sizeof(float) + sizeof(float2)) +
+               (size_t)(B + 1) * sizeof(long long);
     }
     if (pl.max_splits <= 1)
         return 0;
@@ -2165,12 +2191,14 @@ static int decode_impl(const void *q, const void *k_cache, const void *v_cache,
     p.window = window;
     p.out = static_cast<float *>(out);
     p.ws_o = static_cast<float *>(workspace);
+    p.pref = nullptr;
     if (!need) {
         p.ws_ml = nullptr;
     } else if (pl.path == Path::Mma) {
         const size_t slots = (size_t)pl.W + (size_t)batch * pl.units;
         p.ws_ml = reinterpret_cast<float2 *>(static_cast<char *>(workspace) +
                                              slots * pl.sh * D * sizeof(float));
+        p.pref = reinterpret_cast<long long *>(p.ws_ml + slots * pl.sh);
     } else {
         p.ws_ml = reinterpret_cast<float2 *>(static_cast<char *>(workspace) +
                                              (size_t)batch * n_q_heads * pl.max_splits * D *

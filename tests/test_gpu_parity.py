@@ -300,3 +300,16 @@ def test_one_long_unit_spans_every_worker():
     want = oracle_decode(wl, inp)
     got = gpu_decode(wl, to_cuda(inp)).cpu().numpy()
     assert_close(got, want, False, "one long unit")
+
+
+def test_batch_beyond_the_register_scan_publishes_the_prefix():
+    """More than 256 sequences: the split kernel's worker 0 publishes the
+    per-sequence prefix that the merge kernel reads instead of rescanning."""
+    B = 600
+    lens = [(i * 53) % 131 for i in range(B)]
+    lens[7] = 3000
+    wl = W("prefix_published", B, 8, 2, 128, paged=True)
+    inp = build_case(wl, seq_lens=lens, spare_blocks=2)
+    want = oracle_decode(wl, inp)
+    got = gpu_decode(wl, to_cuda(inp)).cpu().numpy()
+    assert_close(got, want, False, "600 sequences")
