@@ -462,6 +462,9 @@ def run_ours(args, world, rank, local):
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": "f32",
+        "math": ("fp16 x fp16 products on the tensor cores (mma.sync), fp32 accumulation and "
+                 "softmax; P rounded to fp16 for the PV product; fp16 K/V"
+                 + (", int8 V x fp16 scale" if wl.v_int8 else "")),
         "data": "synthetic (seeded N(0,1) fp16 q/K/V, random block tables)",
         "config": {"workload": f"{wl.name}: {WORKLOAD_DESCRIPTIONS[wl.name]}",
                    "batch": wl.batch, "n_q_heads": wl.n_q_heads, "n_kv_heads": wl.n_kv_heads,
