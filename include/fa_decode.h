@@ -91,8 +91,14 @@ extern "C" {
  *            ignored when contiguous).
  * workspace  device scratch of at least fa_decode_workspace_size() bytes,
  *            16-byte aligned; contents need no initialisation and are not
- *            preserved.  May be NULL when that size is 0.
- * stream     cudaStream_t to enqueue on.
+ *            preserved.  May be NULL when that size is 0.  Calls that may
+ *            overlap on the GPU must not share a workspace.
+ * stream     cudaStream_t to enqueue on.  A call does all its work in its
+ *            launches on `stream`, and the split plan is made on the device
+ *            from seq_lens and window, so after a first call outside any
+ *            capture (which sets the kernels' shared-memory limits) a call
+ *            may be captured in a CUDA graph and replayed with new
+ *            device-side lengths.
  *
  * q, k_cache, v_cache, v_scales and out must be 16-byte aligned.
  */
