@@ -1366,6 +1366,13 @@ __global__ void __launch_bounds__(Cfg<D, VI8>::NW * 32, 1)
 // flight at once; the per-slot weights ex2(m - M) are computed once into
 // shared memory.
 constexpr int MERGE_THREADS = 256;
+// slots per row whose partial O the merge loads into registers up front
+#ifndef FA_MERGE_REG_SLOTS_128
+#define FA_MERGE_REG_SLOTS_128 32
+#endif
+#ifndef FA_MERGE_REG_SLOTS_256
+#define FA_MERGE_REG_SLOTS_256 64
+#endif
 constexpr int MERGE_MAX_SLOTS = 512;   // per pass over the slots
 
 template <int D>
@@ -1446,10 +1453,25 @@ __global__ void __launch_bounds__(MERGE_THREADS) fa_stream_merge_kernel(const Pa
     const long long u = (long long)b * p.U_b + j;
     const int ns = wl - wf + 1;
 
-    // (m, l) of the slots: loaded once per thread (one slot per thread per
-    // pass of MERGE_THREADS), reduced to M, turned into weights in shared memory
     const int c = tid % CH;
     const int sg = tid / CH;
+    // this thread's O columns of its slots (sg, sg + SG, ...): when they fit
+    // in registers they are loaded before the (m, l) pairs, so both loads are
+    // in flight together and the weights arrive to find them there
+    constexpr int OR = (D == 128 ? FA_MERGE_REG_SLOTS_128 : FA_MERGE_REG_SLOTS_256) / SG;
+    const bool in_regs = OR > 0 && ns <= SG * OR;
+    float4 ov[OR > 0 ? OR : 1];
+    if (in_regs) {
+#pragma unroll
+        for (int k = 0; k < OR; ++k) {
+            const int s = sg + k * SG;
+            ov[k] = s < ns ? reinterpret_cast<const float4 *>(
+                                 p.ws_o + ((wf + s + u) * p.sh + hh) * D)[c]
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    }
+    // (m, l) of the slots: loaded once per thread (one slot per thread per
+    // pass of MERGE_THREADS), reduced to M, turned into weights in shared memory
     float L = 0.f;
     float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
     float M = -INFINITY;
@@ -1492,6 +1514,19 @@ __global__ void __launch_bounds__(MERGE_THREADS) fa_stream_merge_kernel(const Pa
 #pragma unroll
         for (int i = 0; i < MERGE_THREADS / 32; ++i)
             L += red[i];
+        if (in_regs) {
+#pragma unroll
+            for (int k = 0; k < OR; ++k) {
+                const int s = sg + k * SG;
+                if (s < cnt) {
+                    const float a = wgt[s];
+                    o.x = fmaf(ov[k].x, a, o.x);
+                    o.y = fmaf(ov[k].y, a, o.y);
+                    o.z = fmaf(ov[k].z, a, o.z);
+                    o.w = fmaf(ov[k].w, a, o.w);
+                }
+            }
+        } else
 #pragma unroll 4
         for (int s = sg; s < cnt; s += SG) {
             const long long slot = wf + s0 + s + u;
