@@ -270,13 +270,14 @@ def time_kernel(wl, d, steps, warmup, world, device, clocks_gpu=None):
     # the two kernels and stops the merge from overlapping the split's tail)
     ev2 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(steps)]
+    for _, e in ev2:
+        e.record(stream)           # creates the CUDA event before the timed steps
     torch.cuda.synchronize(device)
     for i in range(steps):
         if flush:
             flush(i)
         ev2[i][0].record(stream)
-        ev2[i][1].record(stream)   # creates the event; the library re-records it after the split
-        binding.fa_decode_profile_next(None, ev2[i][1])
+        binding.fa_decode_profile_next(None, ev2[i][1])   # recorded after the split kernel
         call(wl, d, stream)
     torch.cuda.synchronize(device)
     split_ms = [a.elapsed_time(b) for a, b in ev2]
