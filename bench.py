@@ -314,6 +314,49 @@ def time_kernel(wl, d, steps, warmup, world, device, clocks_gpu=None):
     return res
 
 
+BI_SPLIT_TOKENS = (256, 1024)   # split sizes the batch-invariant mode is timed at
+
+
+def time_batch_invariant(wl, d, steps, warmup, device, split_tokens):
+    """fa_decode_batch_invariant on the same inputs and with the same cold-L2
+    protocol as the headline: µs per step."""
+    import torch
+    from decode_step_kv_gb300 import binding
+    from decode_step_kv_gb300.inputs import kv_bytes
+    cap = d["max_blocks"] * (wl.page_size if wl.paged else 1)
+    n = binding.fa_decode_batch_invariant_workspace_size(wl.batch, wl.n_q_heads, wl.n_kv_heads,
+                                                         wl.head_dim, cap, split_tokens)
+    ws = torch.empty(max(n, 16), dtype=torch.uint8, device=device)
+    nbytes = kv_bytes(wl, d["lens"], None if d["window"] is None else d["window"].tolist())
+    flush = L2Flush(device) if nbytes < 4 * L2_BYTES else None
+    stream = torch.cuda.current_stream(device)
+
+    def step():
+        binding.fa_decode_batch_invariant(
+            d["q"], d["k_cache"], d["v_cache"], d["v_scales"], d["block_table"], d["seq_lens"],
+            wl.n_q_heads, wl.n_kv_heads, wl.head_dim, wl.scale, d["window"], d["out"],
+            split_tokens=split_tokens, batch=wl.batch, page_size=wl.page_size,
+            max_blocks_per_seq=d["max_blocks"], num_blocks=d["num_blocks"] if wl.paged else 0,
+            workspace=ws, stream=stream)
+
+    for i in range(warmup):
+        if flush:
+            flush(i)
+        step()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    torch.cuda.synchronize(device)
+    for i in range(steps):
+        if flush:
+            flush(i)
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize(device)
+    del flush
+    return 1e3 * statistics.mean(a.elapsed_time(b) for a, b in ev)
+
+
 def time_e2e(wl, d, steps, warmup, device):
     """Same step through the public API with host inputs: pinned host -> device
     copies of every input, fa_decode, device -> host copy of the output."""
@@ -538,9 +581,18 @@ def run_ours(args, world, rank, local):
                          "l2": rr["l2"]}
             if rr["hot_us_per_step"] is not None:
                 per[name]["hot_l2_us_per_step"] = round(rr["hot_us_per_step"], 2)
+            per[name]["batch_invariant_us_per_step"] = {
+                str(st): round(time_batch_invariant(other, dd, max(10, min(args.steps, 30)), 3,
+                                                    device, st), 2)
+                for st in BI_SPLIT_TOKENS}
             del dd
             torch.cuda.empty_cache()
         line["configs"] = per
+        line["batch_invariant"] = {
+            "split_tokens": list(BI_SPLIT_TOKENS),
+            "note": "configs[*].batch_invariant_us_per_step[split_tokens]: "
+                    "fa_decode_batch_invariant on the same inputs and protocol (fixed splits "
+                    "per sequence, bit-identical whatever the batch)"}
     if rank == 0 and world == 1 and not args.no_cpu:
         inp = cpu_inputs(wl)
         gbs, secs, units, thr = oracle_sample(wl, inp, budget_s=12.0)

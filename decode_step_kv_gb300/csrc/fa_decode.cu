@@ -3,7 +3,7 @@
 //
 // One fa_decode call = two launches on the caller's stream:
 //
-//   tc::fa_stream_mma_kernel<D, int8V>   (the default path)
+//   tc::fa_stream_mma_kernel<D, int8V, BI>   (the default path: BI = false)
 //       Persistent stream-K kernel.  The step's work is flattened into
 //       16-token tiles ordered by (sequence, KV head [x head group], tile);
 //       each warp of the grid owns an equal contiguous range of that space
@@ -14,10 +14,12 @@
 //       share the KV head (up to 8) as the N dimension; the online softmax
 //       sits between them in registers.  At the end of each unit segment the
 //       warp writes the normalised output (it covered the whole unit) or a
-//       partial (O, m, l).
-//   tc::fa_stream_merge_kernel<D>        log-sum-exp merge of the partials,
-//       launched with programmatic dependent launch so it is resident before
-//       the first kernel drains.
+//       partial (O, m, l).  With BI (fa_decode_batch_invariant) the units
+//       are instead cut into fixed chunks that workers take whole, so a
+//       sequence's result does not depend on the rest of the batch.
+//   tc::fa_stream_merge_kernel<D, BI>        log-sum-exp merge of the
+//       partials, launched with programmatic dependent launch so it is
+//       resident before the first kernel drains.
 //
 //   fa_split_kernel<D, GP, int8V> + fa_merge_kernel<D>   (FA_DECODE_KERNEL=simt)
 //       The CUDA-core alternative: one CTA per (split, KV head, sequence),
@@ -100,6 +102,8 @@ struct Params {
     int sh;           // heads stored per workspace slot (stream-K)
     long long *pref;  // stream-K, more than 32*SCAN_REG sequences: [B+1] flattened
                       // start tile of each sequence (last entry: all tiles)
+    int chunk;        // batch-invariant plan: tiles per chunk (0: stream-K plan)
+    int max_chunks;   // batch-invariant plan: chunk slots per unit
 };
 
 // ------------------------------------------------------------ PTX wrappers
@@ -869,6 +873,73 @@ __device__ __forceinline__ long long flat_scan(const Params &p, long long target
     return run;
 }
 
+// Batch-invariant plan: each unit's tiles are cut into chunks of p.chunk
+// tiles counted from its first attended tile, and workers take equal
+// contiguous ranges of whole chunks in (sequence, unit, chunk) order, so what
+// each chunk computes depends on its own sequence alone.  Warp-cooperative
+// scan over the sequences: returns the step's chunks and, through *tiles, its
+// tiles; when target >= 0 also the sequence holding flattened chunk `target`
+// (b_at), that sequence's first flattened tile (P_at) and first flattened
+// chunk (Pc_at).  Every lane returns the same values.
+__device__ __forceinline__ long long chunk_scan(const Params &p, long long target,
+                                                long long *tiles, int &b_at, long long &P_at,
+                                                long long &Pc_at, bool report)
+{
+    const int lane = threadIdx.x & 31;
+    long long run_t = 0, run_c = 0;
+    b_at = -1;
+    P_at = 0;
+    Pc_at = 0;
+    for (int b0 = 0; b0 < p.B; b0 += 32) {
+        const int b = b0 + lane;
+        long long ct = 0, cc = 0;
+        if (b < p.B) {
+            int lo, hi;
+            attended_range(p, b, lo, hi, report);
+            const int n = tiles_in<TILE>(lo, hi);
+            ct = (long long)n * p.U_b;
+            cc = (long long)((n + p.chunk - 1) / p.chunk) * p.U_b;
+        }
+        long long xt = ct, xc = cc;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const long long yt = __shfl_up_sync(0xffffffffu, xt, off);
+            const long long yc = __shfl_up_sync(0xffffffffu, xc, off);
+            if (lane >= off) {
+                xt += yt;
+                xc += yc;
+            }
+        }
+        const long long et = run_t + xt - ct, ec = run_c + xc - cc;
+        if (target >= 0 && b_at < 0) {
+            const unsigned hit =
+                __ballot_sync(0xffffffffu, b < p.B && target >= ec && target < ec + cc);
+            if (hit) {
+                const int src = __ffs(hit) - 1;
+                b_at = b0 + src;
+                P_at = __shfl_sync(0xffffffffu, et, src);
+                Pc_at = __shfl_sync(0xffffffffu, ec, src);
+            }
+        }
+        run_t += __shfl_sync(0xffffffffu, xt, 31);
+        run_c += __shfl_sync(0xffffffffu, xc, 31);
+    }
+    if (tiles)
+        *tiles = run_t;
+    return run_c;
+}
+
+// Flattened tile index of chunk `off` of sequence b (whose first tile is P).
+__device__ __forceinline__ long long chunk_tile(const Params &p, int b, long long P, long long off)
+{
+    int lo, hi;
+    attended_range(p, b, lo, hi, false);
+    const int n = tiles_in<TILE>(lo, hi);
+    const int nch = (n + p.chunk - 1) / p.chunk;
+    const long long j = off / nch;
+    return P + j * n + (off - j * nch) * p.chunk;
+}
+
 // Workers actually used for T tiles (at least MIN_TPW tiles each), and the
 // worker whose contiguous range holds flattened tile t.
 #ifndef FA_MIN_TPW
@@ -931,7 +1002,9 @@ __device__ __forceinline__ void column_range(const Params &p, int b, int L, int 
         lo = static_cast<int>(L - p.cap);
 }
 
-template <int D, bool VI8>
+// BI: the batch-invariant chunk plan instead of stream-K (a separate
+// instantiation, so the default kernel carries none of its code).
+template <int D, bool VI8, bool BI>
 __global__ void __launch_bounds__(Cfg<D, VI8>::NW * 32, 1)
     fa_stream_mma_kernel(const Params p, const __grid_constant__ CUtensorMap tmK,
                          const __grid_constant__ CUtensorMap tmV)
@@ -959,7 +1032,28 @@ __global__ void __launch_bounds__(Cfg<D, VI8>::NW * 32, 1)
     long long P_at = 0;
     long long T, t0, t1;
     int We;
-    if (p.B <= 32 * SCAN_REG) {
+    if constexpr (BI) {
+        // batch-invariant plan: whole chunks per worker; [t0, t1) is the
+        // tile range of chunks [c0, c1)
+        long long Pc;
+        const long long Tc = chunk_scan(p, -1, &T, b_at, P_at, Pc, w == 0);
+        if (Tc == 0)
+            return;
+        We = Tc < p.W ? static_cast<int>(Tc) : p.W;
+        if (w >= We)
+            return;
+        const long long c0 = range_start(w, Tc, We), c1 = range_start(w + 1, Tc, We);
+        chunk_scan(p, c0, nullptr, b_at, P_at, Pc, false);
+        t0 = chunk_tile(p, b_at, P_at, c0 - Pc);
+        if (c1 < Tc) {
+            int b1;
+            long long P1, Pc1;
+            chunk_scan(p, c1, nullptr, b1, P1, Pc1, false);
+            t1 = chunk_tile(p, b1, P1, c1 - Pc1);
+        } else {
+            t1 = T;
+        }
+    } else if (p.B <= 32 * SCAN_REG) {
         // one pass: each lane keeps the tile counts of its sequences
         // (b = lane + 32 i) in registers, then locates t0 from them
         long long c[SCAN_REG], x[SCAN_REG], base[SCAN_REG];
@@ -1291,20 +1385,31 @@ __global__ void __launch_bounds__(Cfg<D, VI8>::NW * 32, 1)
         }
         __syncwarp();
 
-        if (cw.k == cw.n - 1 || i == n_my - 1) {
-            // ---- end of this worker's segment of the unit: publish it
+        if (cw.k == cw.n - 1 || i == n_my - 1 ||
+            (BI && cw.k % p.chunk == p.chunk - 1)) {
+            // ---- end of this worker's segment of the unit (with the
+            // batch-invariant plan: of a chunk): publish it
 #pragma unroll
             for (int mask = 4; mask <= 16; mask <<= 1) {
                 l0 += __shfl_xor_sync(0xffffffffu, l0, mask);
                 l1 += __shfl_xor_sync(0xffffffffu, l1, mask);
             }
-            const long long us = cw.unit_start();
-            const int wf = worker_of(us, T, We);
-            const int wl = worker_of(us + cw.n - 1, T, We);
+            bool whole;          // the segment is the whole unit: normalised output
+            long long slot;      // else its partial's workspace slot
+            if constexpr (BI) {
+                whole = cw.n <= p.chunk;
+                slot = cw.unit(p) * p.max_chunks + cw.k / p.chunk;
+            } else {
+                const long long us = cw.unit_start();
+                const int wf = worker_of(us, T, We);
+                const int wl = worker_of(us + cw.n - 1, T, We);
+                whole = wf == wl;
+                slot = w + cw.unit(p);
+            }
             const int kvu = cw.j / p.n_hg, cgu = cw.j % p.n_hg;
             const int h0 = 2 * t4, h1 = 2 * t4 + 1;   // this lane's columns
             const Col c0 = column(p, kvu, cgu, h0), c1 = column(p, kvu, cgu, h1);
-            if (wf == wl) {
+            if (whole) {
                 // the whole unit was ours: normalised output
                 const float i0 = l0 > 0.f ? 1.f / l0 : 0.f;
                 const float i1 = l1 > 0.f ? 1.f / l1 : 0.f;
@@ -1323,7 +1428,6 @@ __global__ void __launch_bounds__(Cfg<D, VI8>::NW * 32, 1)
                     }
                 }
             } else {
-                const long long slot = w + cw.unit(p);
                 float *o = p.ws_o + slot * p.sh * D;
 #pragma unroll
                 for (int mt = 0; mt < KS; ++mt) {
@@ -1347,7 +1451,8 @@ __global__ void __launch_bounds__(Cfg<D, VI8>::NW * 32, 1)
             reset();
             if (i + 1 < n_my) {
                 cw.next(p);
-                load_q(cw);
+                if (!BI || cw.k == 0)    // a new unit (not just the next chunk)
+                    load_q(cw);
             }
         } else {
             cw.next(p);
@@ -1375,7 +1480,7 @@ constexpr int MERGE_THREADS = 256;
 #endif
 constexpr int MERGE_MAX_SLOTS = 512;   // per pass over the slots
 
-template <int D>
+template <int D, bool BI>
 __global__ void __launch_bounds__(MERGE_THREADS) fa_stream_merge_kernel(const Params p)
 {
     constexpr int CH = D / 4;                    // float4 columns
@@ -1405,53 +1510,66 @@ __global__ void __launch_bounds__(MERGE_THREADS) fa_stream_merge_kernel(const Pa
             reinterpret_cast<float4 *>(p.out + row * D)[tid] = make_float4(0.f, 0.f, 0.f, 0.f);
         return;
     }
-    // T and the flattened start of sequence b: scanned here for up to
-    // 32*SCAN_REG sequences (before the dependency wait, so it overlaps the
-    // split kernel's tail), else published by the split kernel's worker 0
-    __shared__ long long sh_T, sh_P;
-    const bool scan_here = p.B <= 32 * SCAN_REG;
-    if (scan_here && wid == 0) {
-        int b_at;
-        long long P_at;
-        const long long T = flat_scan(p, -1, b_at, P_at);
-        long long run = 0;
-        for (int b0 = 0; b0 < b; b0 += 32) {
-            const int bb = b0 + lane;
-            long long c = 0;
-            if (bb < b) {
-                int l2, h2;
-                attended_range(p, bb, l2, h2, false);
-                c = (long long)tiles_in<TILE>(l2, h2) * p.U_b;
-            }
-#pragma unroll
-            for (int off = 16; off >= 1; off >>= 1)
-                c += __shfl_xor_sync(0xffffffffu, c, off);
-            run += c;
-        }
-        if (lane == 0) {
-            sh_T = T;
-            sh_P = run;
-        }
-    }
-    if (!scan_here) {
-        asm volatile("griddepcontrol.wait;" ::: "memory");
-        if (tid == 0) {
-            sh_T = p.pref[p.B];
-            sh_P = p.pref[b];
-        }
-    }
-    __syncthreads();
-    const long long T = sh_T;
-    const int We = workers_for(p, T);
-    const long long us = sh_P + (long long)j * n;
-    const int wf = worker_of(us, T, We);
-    const int wl = worker_of(us + n - 1, T, We);
-    if (wf == wl)
-        return;                                   // written by the split kernel
-    if (scan_here)
-        asm volatile("griddepcontrol.wait;" ::: "memory");
     const long long u = (long long)b * p.U_b + j;
-    const int ns = wl - wf + 1;
+    long long sb;    // workspace slot of the row's first partial
+    int ns;          // partials to fold, in slot order
+    if constexpr (BI) {
+        // batch-invariant plan: the unit's chunks, one slot each
+        ns = (n + p.chunk - 1) / p.chunk;
+        if (ns == 1)
+            return;                               // written by the split kernel
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        sb = u * p.max_chunks;
+    } else {
+        // T and the flattened start of sequence b: scanned here for up to
+        // 32*SCAN_REG sequences (before the dependency wait, so it overlaps
+        // the split kernel's tail), else published by the split kernel's
+        // worker 0
+        __shared__ long long sh_T, sh_P;
+        const bool scan_here = p.B <= 32 * SCAN_REG;
+        if (scan_here && wid == 0) {
+            int b_at;
+            long long P_at;
+            const long long T = flat_scan(p, -1, b_at, P_at);
+            long long run = 0;
+            for (int b0 = 0; b0 < b; b0 += 32) {
+                const int bb = b0 + lane;
+                long long c = 0;
+                if (bb < b) {
+                    int l2, h2;
+                    attended_range(p, bb, l2, h2, false);
+                    c = (long long)tiles_in<TILE>(l2, h2) * p.U_b;
+                }
+#pragma unroll
+                for (int off = 16; off >= 1; off >>= 1)
+                    c += __shfl_xor_sync(0xffffffffu, c, off);
+                run += c;
+            }
+            if (lane == 0) {
+                sh_T = T;
+                sh_P = run;
+            }
+        }
+        if (!scan_here) {
+            asm volatile("griddepcontrol.wait;" ::: "memory");
+            if (tid == 0) {
+                sh_T = p.pref[p.B];
+                sh_P = p.pref[b];
+            }
+        }
+        __syncthreads();
+        const long long T = sh_T;
+        const int We = workers_for(p, T);
+        const long long us = sh_P + (long long)j * n;
+        const int wf = worker_of(us, T, We);
+        const int wl = worker_of(us + n - 1, T, We);
+        if (wf == wl)
+            return;                               // written by the split kernel
+        if (scan_here)
+            asm volatile("griddepcontrol.wait;" ::: "memory");
+        sb = wf + u;
+        ns = wl - wf + 1;
+    }
 
     const int c = tid % CH;
     const int sg = tid / CH;
@@ -1466,7 +1584,7 @@ __global__ void __launch_bounds__(MERGE_THREADS) fa_stream_merge_kernel(const Pa
         for (int k = 0; k < OR; ++k) {
             const int s = sg + k * SG;
             ov[k] = s < ns ? reinterpret_cast<const float4 *>(
-                                 p.ws_o + ((wf + s + u) * p.sh + hh) * D)[c]
+                                 p.ws_o + ((sb + s) * p.sh + hh) * D)[c]
                            : make_float4(0.f, 0.f, 0.f, 0.f);
         }
     }
@@ -1478,11 +1596,11 @@ __global__ void __launch_bounds__(MERGE_THREADS) fa_stream_merge_kernel(const Pa
     float2 mine = make_float2(-INFINITY, 0.f);
     if (ns <= MERGE_THREADS) {
         if (tid < ns)
-            mine = p.ws_ml[(wf + tid + u) * p.sh + hh];
+            mine = p.ws_ml[(sb + tid) * p.sh + hh];
         M = mine.x;
     } else {
         for (int s = tid; s < ns; s += MERGE_THREADS)
-            M = fmaxf(M, p.ws_ml[(wf + s + u) * p.sh + hh].x);
+            M = fmaxf(M, p.ws_ml[(sb + s) * p.sh + hh].x);
     }
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1)
@@ -1500,7 +1618,7 @@ __global__ void __launch_bounds__(MERGE_THREADS) fa_stream_merge_kernel(const Pa
         const int cnt = min(MERGE_MAX_SLOTS, ns - s0);
         float Lp = 0.f;
         for (int s = tid; s < cnt; s += MERGE_THREADS) {
-            const float2 v = (ns <= MERGE_THREADS) ? mine : p.ws_ml[(wf + s0 + s + u) * p.sh + hh];
+            const float2 v = (ns <= MERGE_THREADS) ? mine : p.ws_ml[(sb + s0 + s) * p.sh + hh];
             const float a = (v.x == -INFINITY) ? 0.f : ex2(v.x - M);
             wgt[s] = a;
             Lp = fmaf(v.y, a, Lp);
@@ -1529,7 +1647,7 @@ __global__ void __launch_bounds__(MERGE_THREADS) fa_stream_merge_kernel(const Pa
         } else
 #pragma unroll 4
         for (int s = sg; s < cnt; s += SG) {
-            const long long slot = wf + s0 + s + u;
+            const long long slot = sb + s0 + s;
             const float4 x =
                 reinterpret_cast<const float4 *>(p.ws_o + (slot * p.sh + hh) * D)[c];
             const float a = wgt[s];
@@ -1756,6 +1874,8 @@ struct Plan {
     int units;       // units per sequence (kv heads x head groups)
     int tps;         // tiles per split
     int max_splits;
+    int chunk;       // batch-invariant plan: tiles per chunk (0: stream-K)
+    int max_chunks;  // batch-invariant plan: chunk slots per unit
 };
 
 static int next_pow2(int x)
@@ -1782,7 +1902,7 @@ static Path choose_path()
 // grid holds several waves of resident CTAs (the "nwg" of the pages, chosen
 // here from the SM count rather than a fixed bucket).
 static Plan make_plan(Path path, int B, int Hq, int Hkv, int D, long long cap, int num_sms,
-                      bool vi8, int tq = 1)
+                      bool vi8, int tq = 1, int chunk = 0)
 {
     Plan pl = {};
     pl.path = path;
@@ -1808,6 +1928,14 @@ static Plan make_plan(Path path, int B, int Hq, int Hkv, int D, long long cap, i
         pl.W = pl.ctas * nw;
         pl.tps = 0;
         pl.max_splits = 0;
+        if (chunk > 0) {
+            // a unit holds at most ceil(cap / 16) tiles
+            const long long max_tiles = (cap + tc::TILE - 1) / tc::TILE;
+            pl.chunk = chunk;
+            pl.max_chunks = static_cast<int>((max_tiles + chunk - 1) / chunk);
+            if (pl.max_chunks < 1)
+                pl.max_chunks = 1;
+        }
         return pl;
     } else {
         pl.tile = 2048 / D;
@@ -1838,6 +1966,11 @@ static Plan make_plan(Path path, int B, int Hq, int Hkv, int D, long long cap, i
 
 static size_t plan_workspace(const Plan &pl, int B, int Hq, int D)
 {
+    if (pl.path == Path::Mma && pl.chunk > 0) {
+        // batch-invariant plan: one partial slot per (unit, chunk)
+        const size_t slots = (size_t)B * pl.units * pl.max_chunks;
+        return slots * pl.sh * (D * sizeof(float) + sizeof(float2));
+    }
     if (pl.path == Path::Mma) {
         // partial slots: one per (worker, unit) pair, at most W + units
         (void)Hq;
@@ -1956,7 +2089,7 @@ static int encode_kv_map(CUtensorMap *map, const void *base, long long rows, int
     return 0;
 }
 
-template <int D, bool VI8>
+template <int D, bool VI8, bool BI>
 static cudaError_t launch_mma(const Params &p, const CUtensorMap &tmK, const CUtensorMap &tmV,
                               dim3 grid, cudaStream_t st)
 {
@@ -1970,7 +2103,7 @@ static cudaError_t launch_mma(const Params &p, const CUtensorMap &tmK, const CUt
     {
         std::lock_guard<std::mutex> lock(mu);
         if (dev >= 64 || !done[dev]) {
-            e = cudaFuncSetAttribute(tc::fa_stream_mma_kernel<D, VI8>,
+            e = cudaFuncSetAttribute(tc::fa_stream_mma_kernel<D, VI8, BI>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
             if (e != cudaSuccess)
                 return e;
@@ -1978,7 +2111,8 @@ static cudaError_t launch_mma(const Params &p, const CUtensorMap &tmK, const CUt
                 done[dev] = true;
         }
     }
-    tc::fa_stream_mma_kernel<D, VI8><<<grid, tc::Cfg<D, VI8>::NW * 32, smem, st>>>(p, tmK, tmV);
+    tc::fa_stream_mma_kernel<D, VI8, BI><<<grid, tc::Cfg<D, VI8>::NW * 32, smem, st>>>(p, tmK,
+                                                                                     tmV);
     return cudaGetLastError();
 }
 
@@ -2063,7 +2197,8 @@ static int decode_impl(const void *q, const void *k_cache, const void *v_cache,
                        const int32_t *seq_lens, int n_q_heads, int n_kv_heads, int head_dim,
                        float scale, const int32_t *window, void *out, int batch, int page_size,
                        int max_blocks_per_seq, int num_blocks, void *workspace,
-                       size_t workspace_bytes, void *stream, bool ring, int tq);
+                       size_t workspace_bytes, void *stream, bool ring, int tq,
+                       int chunk = 0);
 
 FA_API int fa_decode(const void *q, const void *k_cache, const void *v_cache,
                      const void *v_scales, const int32_t *block_table,
@@ -2075,6 +2210,41 @@ FA_API int fa_decode(const void *q, const void *k_cache, const void *v_cache,
     return decode_impl(q, k_cache, v_cache, v_scales, block_table, seq_lens, n_q_heads,
                        n_kv_heads, head_dim, scale, window, out, batch, page_size,
                        max_blocks_per_seq, num_blocks, workspace, workspace_bytes, stream, false, 1);
+}
+
+static bool split_tokens_ok(int split_tokens)
+{
+    return split_tokens > 0 && split_tokens % 16 == 0 && split_tokens <= (1 << 30);
+}
+
+FA_API int fa_decode_batch_invariant(const void *q, const void *k_cache, const void *v_cache,
+                                     const void *v_scales, const int32_t *block_table,
+                                     const int32_t *seq_lens, int n_q_heads, int n_kv_heads,
+                                     int head_dim, float scale, const int32_t *window, void *out,
+                                     int batch, int page_size, int max_blocks_per_seq,
+                                     int num_blocks, int split_tokens, void *workspace,
+                                     size_t workspace_bytes, void *stream)
+{
+    g_err[0] = 0;
+    if (!split_tokens_ok(split_tokens))
+        return fail(FA_ERR_LAYOUT, "fa_decode_batch_invariant: split_tokens %d must be a "
+                                   "positive multiple of 16", split_tokens);
+    return decode_impl(q, k_cache, v_cache, v_scales, block_table, seq_lens, n_q_heads,
+                       n_kv_heads, head_dim, scale, window, out, batch, page_size,
+                       max_blocks_per_seq, num_blocks, workspace, workspace_bytes, stream, false, 1,
+                       split_tokens / 16);
+}
+
+FA_API size_t fa_decode_batch_invariant_workspace_size(int batch, int n_q_heads, int n_kv_heads,
+                                                       int head_dim, int max_kv_len,
+                                                       int split_tokens)
+{
+    if (batch <= 0 || n_q_heads <= 0 || n_kv_heads <= 0 || n_q_heads % n_kv_heads ||
+        (head_dim != 128 && head_dim != 256) || max_kv_len < 0 || !split_tokens_ok(split_tokens))
+        return 0;
+    const Plan pl = make_plan(Path::Mma, batch, n_q_heads, n_kv_heads, head_dim, max_kv_len, 1,
+                              false, 1, split_tokens / 16);
+    return plan_workspace(pl, batch, n_q_heads, head_dim);
 }
 
 FA_API int fa_decode_multi(const void *q, const void *k_cache, const void *v_cache,
@@ -2137,7 +2307,7 @@ static int decode_impl(const void *q, const void *k_cache, const void *v_cache,
                        const int32_t *seq_lens, int n_q_heads, int n_kv_heads, int head_dim,
                        float scale, const int32_t *window, void *out, int batch, int page_size,
                        int max_blocks_per_seq, int num_blocks, void *workspace,
-                       size_t workspace_bytes, void *stream, bool ring, int tq)
+                       size_t workspace_bytes, void *stream, bool ring, int tq, int chunk)
 {
     g_err[0] = 0;
     if (!q || !k_cache || !v_cache || !seq_lens || !out)
@@ -2197,16 +2367,18 @@ static int decode_impl(const void *q, const void *k_cache, const void *v_cache,
     const long long kv_rows_total = paged ? (long long)num_blocks * n_kv_heads * page_size
                                           : (long long)batch * n_kv_heads * cap;
     if (kv_rows_total >= (1ll << 31)) {
-        if (tq > 1)
-            return fail(FA_ERR_LAYOUT, "fa_decode_multi: caches of 2^31 rows or more are not "
-                                       "supported with several queries");
+        if (tq > 1 || chunk > 0)
+            return fail(FA_ERR_LAYOUT, "fa_decode: caches of 2^31 rows or more are not "
+                                       "supported with several queries or batch-invariant "
+                                       "splits");
         path = Path::Simt;   // TMA row coordinates are 32-bit
     }
-    if (tq > 1)
-        path = Path::Mma;    // only the tensor-core kernel has per-column query ranges
+    if (tq > 1 || chunk > 0)
+        path = Path::Mma;    // only the tensor-core kernel has per-column query ranges and
+                             // the chunk plan
     // a ring's attended range (the last cap tokens) can straddle one more tile
     const Plan pl = make_plan(path, batch, n_q_heads, n_kv_heads, D, ring ? cap + 16 : cap, sms,
-                              vi8, tq);
+                              vi8, tq, chunk);
     const size_t need = plan_workspace(pl, batch, n_q_heads, D);
     if (need > 0 && (!workspace || workspace_bytes < need))
         return fail(FA_ERR_WORKSPACE, "fa_decode: workspace %zu bytes, need %zu", workspace_bytes,
@@ -2216,7 +2388,7 @@ static int decode_impl(const void *q, const void *k_cache, const void *v_cache,
     if (batch == 0)
         return 0;
 
-    Params p;
+    Params p = {};
     p.q = static_cast<const __half *>(q);
     p.k = static_cast<const char *>(k_cache);
     p.v = static_cast<const char *>(v_cache);
@@ -2229,6 +2401,10 @@ static int decode_impl(const void *q, const void *k_cache, const void *v_cache,
     p.pref = nullptr;
     if (!need) {
         p.ws_ml = nullptr;
+    } else if (pl.path == Path::Mma && pl.chunk > 0) {
+        const size_t slots = (size_t)batch * pl.units * pl.max_chunks;
+        p.ws_ml = reinterpret_cast<float2 *>(static_cast<char *>(workspace) +
+                                             slots * pl.sh * D * sizeof(float));
     } else if (pl.path == Path::Mma) {
         const size_t slots = (size_t)pl.W + (size_t)batch * pl.units;
         p.ws_ml = reinterpret_cast<float2 *>(static_cast<char *>(workspace) +
@@ -2258,6 +2434,8 @@ static int decode_impl(const void *q, const void *k_cache, const void *v_cache,
     p.W = pl.W;
     p.U_b = n_kv_heads * pl.n_hg;
     p.sh = pl.sh;
+    p.chunk = pl.chunk;
+    p.max_chunks = pl.max_chunks;
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const dim3 grid = pl.path == Path::Mma ? dim3(pl.ctas)
@@ -2276,14 +2454,22 @@ static int decode_impl(const void *q, const void *k_cache, const void *v_cache,
             return rk;
         if (vi8) {
             tmV = tmK;   // unused: int8 V arrives by plain bulk copies
-            e = D == 128 ? launch_mma<128, true>(p, tmK, tmV, grid, st)
-                         : launch_mma<256, true>(p, tmK, tmV, grid, st);
+            if (pl.chunk > 0)
+                e = D == 128 ? launch_mma<128, true, true>(p, tmK, tmV, grid, st)
+                             : launch_mma<256, true, true>(p, tmK, tmV, grid, st);
+            else
+                e = D == 128 ? launch_mma<128, true, false>(p, tmK, tmV, grid, st)
+                             : launch_mma<256, true, false>(p, tmK, tmV, grid, st);
         } else {
             const int rv = encode_kv_map(&tmV, v_cache, kv_rows_total, D);
             if (rv)
                 return rv;
-            e = D == 128 ? launch_mma<128, false>(p, tmK, tmV, grid, st)
-                         : launch_mma<256, false>(p, tmK, tmV, grid, st);
+            if (pl.chunk > 0)
+                e = D == 128 ? launch_mma<128, false, true>(p, tmK, tmV, grid, st)
+                             : launch_mma<256, false, true>(p, tmK, tmV, grid, st);
+            else
+                e = D == 128 ? launch_mma<128, false, false>(p, tmK, tmV, grid, st)
+                             : launch_mma<256, false, false>(p, tmK, tmV, grid, st);
         }
     } else if (e == cudaSuccess) {
         if (D == 128)
@@ -2311,8 +2497,11 @@ static int decode_impl(const void *q, const void *k_cache, const void *v_cache,
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         if (pl.path == Path::Mma)
-            e = D == 128 ? cudaLaunchKernelEx(&cfg, tc::fa_stream_merge_kernel<128>, p)
-                         : cudaLaunchKernelEx(&cfg, tc::fa_stream_merge_kernel<256>, p);
+            e = pl.chunk > 0
+                    ? (D == 128 ? cudaLaunchKernelEx(&cfg, tc::fa_stream_merge_kernel<128, true>, p)
+                                : cudaLaunchKernelEx(&cfg, tc::fa_stream_merge_kernel<256, true>, p))
+                    : (D == 128 ? cudaLaunchKernelEx(&cfg, tc::fa_stream_merge_kernel<128, false>, p)
+                                : cudaLaunchKernelEx(&cfg, tc::fa_stream_merge_kernel<256, false>, p));
         else
             e = D == 128 ? cudaLaunchKernelEx(&cfg, fa_merge_kernel<128>, p)
                          : cudaLaunchKernelEx(&cfg, fa_merge_kernel<256>, p);
@@ -2381,7 +2570,7 @@ FA_API int fa_append_kv(const float *k_new, const float *v_new, void *k_cache, v
         return fail(FA_ERR_LAYOUT, "fa_append_kv: too many rows");
     if (batch == 0)
         return 0;
-    Params p;
+    Params p = {};
     memset(&p, 0, sizeof(p));
     p.bt = block_table;
     p.seq_lens = positions;
@@ -2427,7 +2616,7 @@ FA_API int fa_append_kv_ring(const float *k_new, const float *v_new, void *k_cac
         return fail(FA_ERR_LAYOUT, "fa_append_kv_ring: too many rows");
     if (batch == 0)
         return 0;
-    Params p;
+    Params p = {};
     memset(&p, 0, sizeof(p));
     p.seq_lens = positions;
     p.B = batch;
@@ -2462,7 +2651,7 @@ FA_API int fa_gather_kv_debug(const void *cache, int row_bytes, const int32_t *b
                     cap);
     if (n_tokens == 0)
         return 0;
-    Params p;
+    Params p = {};
     memset(&p, 0, sizeof(p));
     p.k = static_cast<const char *>(cache);
     p.bt = block_table;

@@ -110,6 +110,44 @@ FA_API int fa_decode(const void *q, const void *k_cache, const void *v_cache,
                      size_t workspace_bytes, void *stream);
 
 /*
+ * fa_decode_batch_invariant -- fa_decode whose result for a sequence does not
+ * depend on the rest of the batch, bit for bit: a sequence decoded alone,
+ * or in any batch, in any position, gives the same bytes.  The pages hold
+ * their batched kernels to this rule against serial single-slot runs
+ * (batched-vs-serial parity).
+ *
+ * fa_decode's split plan gives every worker an equal share of the whole
+ * batch's tiles, so where a sequence's KV range is cut, and so the rounding
+ * of its merged result, depends on the batch.  Here each (sequence, KV head
+ * [, head group]) range is cut into splits of split_tokens keys counted from
+ * its first attended key, whatever the batch.  Each split is computed from
+ * scratch by one worker.  The splits' partials are merged in split order.
+ * Workers take equal runs of whole splits, so the balance is coarser than
+ * fa_decode's; a sequence of at most split_tokens keys is not split at all.
+ *
+ * split_tokens  a positive multiple of 16: keys per split (e.g. 512).
+ * workspace     fa_decode_batch_invariant_workspace_size() bytes; contents
+ *               need no initialisation.
+ * Other arguments, layouts, rules and errors as fa_decode, plus
+ * FA_ERR_LAYOUT for a bad split_tokens.  The result equals fa_decode's
+ * within the same tolerances.
+ */
+FA_API int fa_decode_batch_invariant(const void *q, const void *k_cache, const void *v_cache,
+                                     const void *v_scales, const int32_t *block_table,
+                                     const int32_t *seq_lens, int n_q_heads, int n_kv_heads,
+                                     int head_dim, float scale, const int32_t *window, void *out,
+                                     int batch, int page_size, int max_blocks_per_seq,
+                                     int num_blocks, int split_tokens, void *workspace,
+                                     size_t workspace_bytes, void *stream);
+
+/* Scratch bytes for fa_decode_batch_invariant: one partial (D floats of O
+ * plus max and sum) per query head and split of every sequence at
+ * max_kv_len keys.  Host-only; 0 for invalid sizes. */
+FA_API size_t fa_decode_batch_invariant_workspace_size(int batch, int n_q_heads, int n_kv_heads,
+                                                       int head_dim, int max_kv_len,
+                                                       int split_tokens);
+
+/*
  * fa_decode_multi -- several query tokens per sequence in one call: the
  * speculative-verify form of the decode step (the n_queries field of the
  * pages' params; causal rule of tessl's flash_attn_rows on the "nn.rs" page).

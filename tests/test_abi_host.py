@@ -145,3 +145,23 @@ def test_multi_rejects_bad_query_count_and_sizes_its_workspace(lib):
     assert g(1, 0, 8, 2, 128, 512, 152) == 0
     assert g(1, 1, 8, 2, 128, 512, 152) == lib.fa_decode_workspace_size(1, 8, 2, 128, 512, 152)
     assert g(2, 4, 8, 2, 128, 512, 152) >= g(2, 1, 8, 2, 128, 512, 152)
+
+
+def test_batch_invariant_rejects_bad_split_and_sizes_its_workspace(lib):
+    f = lib.fa_decode_batch_invariant
+    #                q  k      v      vs    bt    sl     hq hkv d   scale win  out    B  P   maxb nblk
+    args = lambda st: (A, 2 * A, 3 * A, None, None, 4 * A, 8, 2, 128, 0.1, None, 5 * A, 1, 16, 512, 0,
+                       st, 6 * A, 1 << 30, None)
+    for bad in (0, -16, 24, 8):
+        assert f(*args(bad)) == -6, bad
+        assert lib.fa_decode_last_error()
+    g = lib.fa_decode_batch_invariant_workspace_size
+    assert g(1, 8, 2, 128, 512, 0) == 0 and g(1, 8, 2, 128, 512, 8) == 0
+    assert g(0, 8, 2, 128, 512, 512) == 0 and g(1, 6, 4, 128, 512, 512) == 0
+    # one partial (D floats of O + max and sum) per query head of each unit
+    # (2 KV heads x 4 heads) and split: 512 keys in 512-key splits is one
+    one = g(1, 8, 2, 128, 512, 512)
+    assert one == 2 * 1 * 4 * (128 * 4 + 8)
+    assert g(1, 8, 2, 128, 512, 16) == 32 * one
+    assert g(3, 8, 2, 128, 512, 512) == 3 * one
+    assert g(1, 8, 2, 128, 513, 512) == 2 * one

@@ -1,0 +1,109 @@
+"""GPU checks of fa_decode_batch_invariant.
+
+Each sequence's KV range is cut into splits of a fixed number of keys, so a
+sequence's output must be the same bytes however it is batched: alone, in
+another order, or beside other sequences (the pages' batched-vs-serial
+parity rule).  The outputs also match the fp64 oracle within the usual
+tolerances.
+"""
+import zlib
+
+import numpy as np
+import pytest
+import torch
+
+from decode_step_kv_gb300 import binding
+from decode_step_kv_gb300.inputs import Workload
+
+from _helpers import assert_close, build_case, oracle_decode, to_cuda
+
+pytestmark = pytest.mark.gpu
+
+
+def W(name, B, Hq, Hkv, D, **kw):
+    return Workload(name, B, Hq, Hkv, D, seed=9500 + zlib.crc32(name.encode()) % 1000, **kw)
+
+
+def _run(wl, dinp, split_tokens, rows=None):
+    """Decode sequences `rows` (default: all) of the case as one batch."""
+    rows = list(range(wl.batch)) if rows is None else list(rows)
+    idx = torch.tensor(rows, device="cuda")
+    q = dinp["q"].index_select(0, idx).contiguous()
+    sl = dinp["seq_lens"].index_select(0, idx).contiguous()
+    bt = None if dinp["block_table"] is None else dinp["block_table"].index_select(0, idx).contiguous()
+    win = None if dinp["window"] is None else dinp["window"].index_select(0, idx).contiguous()
+    k, v, vs = dinp["k_cache"], dinp["v_cache"], dinp.get("v_scales")
+    if not wl.paged:        # contiguous caches are indexed by position in the batch
+        k = k.index_select(0, idx).contiguous()
+        v = v.index_select(0, idx).contiguous()
+        vs = None if vs is None else vs.index_select(0, idx).contiguous()
+    B = len(rows)
+    cap = dinp["max_blocks"] * (wl.page_size if wl.paged else 1)
+    n = binding.fa_decode_batch_invariant_workspace_size(B, wl.n_q_heads, wl.n_kv_heads,
+                                                         wl.head_dim, cap, split_tokens)
+    ws = torch.empty(max(n, 16), dtype=torch.uint8, device="cuda")
+    ws.fill_(0xFF)
+    out = torch.full((B, wl.n_q_heads, wl.head_dim), float("nan"), device="cuda")
+    binding.fa_decode_batch_invariant(q, k, v, vs, bt, sl, wl.n_q_heads, wl.n_kv_heads,
+                                      wl.head_dim, wl.scale, win, out, split_tokens=split_tokens,
+                                      batch=B, page_size=wl.page_size,
+                                      max_blocks_per_seq=dinp["max_blocks"],
+                                      num_blocks=dinp["num_blocks"] if wl.paged else 0,
+                                      workspace=ws)
+    torch.cuda.synchronize()
+    return out.cpu()
+
+
+CASES = [
+    (W("bi_d128_paged", 6, 8, 2, 128, paged=True), [1, 15, 700, 3000, 0, 9000], 512),
+    (W("bi_d128_contig_win", 5, 16, 2, 128, window=300, window_odd_only=True),
+     [17, 2000, 2000, 513, 4096], 256),
+    (W("bi_d256_paged", 4, 8, 4, 256, paged=True), [33, 1024, 5000, 7], 64),
+    (W("bi_d256_int8", 4, 8, 2, 256, paged=True, v_int8=True), [2500, 9, 1200, 4000], 512),
+    (W("bi_d128_int8_g8", 3, 32, 4, 128, paged=True, v_int8=True, window=1000),
+     [6000, 999, 1001], 128),
+    (W("bi_d128_split16", 3, 4, 4, 128, paged=True), [100, 257, 40], 16),
+]
+
+
+@pytest.mark.parametrize("wl,lens,st", CASES, ids=[c[0].name for c in CASES])
+def test_matches_oracle(wl, lens, st):
+    inp = build_case(wl, seq_lens=lens, spare_blocks=2 if wl.paged else 0)
+    got = _run(wl, to_cuda(inp), st).numpy()
+    assert_close(got, oracle_decode(wl, inp), wl.v_int8, wl.name)
+    for b, L in enumerate(lens):
+        if L == 0:
+            assert np.all(got[b] == 0)
+
+
+@pytest.mark.parametrize("wl,lens,st", CASES, ids=[c[0].name for c in CASES])
+def test_each_sequence_alone_in_another_order_and_in_a_bigger_batch_bitwise(wl, lens, st):
+    inp = build_case(wl, seq_lens=lens, spare_blocks=2 if wl.paged else 0)
+    dinp = to_cuda(inp)
+    whole = _run(wl, dinp, st)
+    for b in range(wl.batch):
+        alone = _run(wl, dinp, st, rows=[b])
+        assert torch.equal(alone[0], whole[b]), f"sequence {b} alone"
+    perm = list(reversed(range(wl.batch)))
+    shuffled = _run(wl, dinp, st, rows=perm)
+    for i, b in enumerate(perm):
+        assert torch.equal(shuffled[i], whole[b]), f"sequence {b} reordered"
+    twice = _run(wl, dinp, st, rows=list(range(wl.batch)) * 2)
+    assert torch.equal(twice[:wl.batch], whole) and torch.equal(twice[wl.batch:], whole)
+
+
+def test_stream_k_plan_is_batch_dependent_but_close():
+    """For contrast: fa_decode's plan cuts a sequence where the batch puts the
+    worker boundaries, so its bytes may change with the batch; the results
+    still agree within the tolerances."""
+    wl, lens, st = CASES[0]
+    inp = build_case(wl, seq_lens=lens, spare_blocks=2)
+    dinp = to_cuda(inp)
+    inv = _run(wl, dinp, st).numpy()
+    cap = dinp["max_blocks"] * wl.page_size
+    ws = binding.alloc_workspace(wl.batch, wl.n_q_heads, wl.n_kv_heads, wl.head_dim, cap)
+    out = torch.empty((wl.batch, wl.n_q_heads, wl.head_dim), device="cuda")
+    binding.fa_decode(dinp["q"], dinp["k_cache"], dinp["v_cache"], None, dinp["block_table"],
+                      dinp["seq_lens"], wl.n_q_heads, wl.n_kv_heads, wl.head_dim, wl.scale, None,
+                      out, workspace=ws)
+    assert_close(out.cpu().numpy(), inv, False, "stream-K vs batch-invariant")
