@@ -112,9 +112,9 @@ FA_API int fa_decode(const void *q, const void *k_cache, const void *v_cache,
 /*
  * fa_decode_batch_invariant -- fa_decode whose result for a sequence does not
  * depend on the rest of the batch, bit for bit: a sequence decoded alone,
- * or in any batch, in any position, gives the same bytes.  The pages hold
- * their batched kernels to this rule against serial single-slot runs
- * (batched-vs-serial parity).
+ * or in any batch, in any position, gives the same bytes.  The hf2q page
+ * "batched_body.rs" holds its batched multi-slot decode to this rule against
+ * serial single-slot runs (its slot-aware parity tests).
  *
  * fa_decode's split plan gives every worker an equal share of the whole
  * batch's tiles, so where a sequence's KV range is cut, and so the rounding
