@@ -1217,6 +1217,7 @@ __global__ void __launch_bounds__(Cfg<D, VI8>::NW * 32, 1)
     reset();
 
     int i_fail = -1;
+    int ck = 0;     // batch-invariant plan: tile within the chunk (ranges start on a chunk)
     for (int i = 0; i < n_my; ++i) {
         const int s = i % STAGES;
         if (!mbar_wait_warp(my_bars + 8 * s, (i / STAGES) & 1)) {
@@ -1386,7 +1387,7 @@ __global__ void __launch_bounds__(Cfg<D, VI8>::NW * 32, 1)
         __syncwarp();
 
         if (cw.k == cw.n - 1 || i == n_my - 1 ||
-            (BI && cw.k % p.chunk == p.chunk - 1)) {
+            (BI && ck == p.chunk - 1)) {
             // ---- end of this worker's segment of the unit (with the
             // batch-invariant plan: of a chunk): publish it
 #pragma unroll
@@ -1454,8 +1455,10 @@ __global__ void __launch_bounds__(Cfg<D, VI8>::NW * 32, 1)
                 if (!BI || cw.k == 0)    // a new unit (not just the next chunk)
                     load_q(cw);
             }
+            ck = 0;
         } else {
             cw.next(p);
+            ++ck;
         }
     }
     if (i_fail >= 0)
