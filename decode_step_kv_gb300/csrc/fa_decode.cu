@@ -1474,6 +1474,10 @@ __global__ void __launch_bounds__(Cfg<D, VI8>::NW * 32, 1)
 // flight at once; the per-slot weights ex2(m - M) are computed once into
 // shared memory.
 constexpr int MERGE_THREADS = 256;
+// rows per SM from which the stream-K merge takes a warp per row
+#ifndef FA_MERGE_WARP_ROWS_PER_SM
+#define FA_MERGE_WARP_ROWS_PER_SM 4
+#endif
 // slots per row whose partial O the merge loads into registers up front
 #ifndef FA_MERGE_REG_SLOTS_128
 #define FA_MERGE_REG_SLOTS_128 32
@@ -1676,6 +1680,123 @@ __global__ void __launch_bounds__(MERGE_THREADS) fa_stream_merge_kernel(const Pa
         reinterpret_cast<float4 *>(p.out + row * D)[c] =
             make_float4(o.x * inv, o.y * inv, o.z * inv, o.w * inv);
     }
+}
+
+// Warp-per-row form of the stream-K merge, for steps with many rows (the
+// host picks it at four or more rows per SM): eight rows per CTA, so the
+// grid runs in fewer, fuller waves and every row's length scan is one warp's
+// work.  Each lane owns D/128 float4 columns of the row; the slots' weights
+// are computed 32 at a time, one per lane, and broadcast by shuffles while
+// the partial O columns stream in.  The fold runs in slot order.
+constexpr int MERGE_ROWS_PER_CTA = 8;
+
+template <int D>
+__global__ void __launch_bounds__(MERGE_ROWS_PER_CTA * 32) fa_stream_merge_rows_kernel(
+    const Params p)
+{
+    constexpr int CPL = D / 128;                 // float4 columns per lane
+    const int lane = threadIdx.x & 31;
+    const int tq = p.tq > 1 ? p.tq : 1;
+    const long long rows = (long long)p.B * tq * p.Hq;
+    const long long row = (long long)blockIdx.x * MERGE_ROWS_PER_CTA + (threadIdx.x >> 5);
+    if (row >= rows)
+        return;
+    // row = (b * tq + query) * Hq + head; its column x = query * G + head % G
+    const int b = static_cast<int>(row / ((long long)tq * p.Hq));
+    const int qj = static_cast<int>((row / p.Hq) % tq);
+    const int h = static_cast<int>(row % p.Hq);
+    const int kv = h / p.G;
+    const int x = qj * p.G + h % p.G;
+    const int j = kv * p.n_hg + x / GPH;
+    const int hh = x % GPH;
+    float4 *dst = reinterpret_cast<float4 *>(p.out + row * D);
+
+    int lo, hi;
+    attended_range(p, b, lo, hi, false);
+    const int n = tiles_in<TILE>(lo, hi);
+    if (n == 0) {
+#pragma unroll
+        for (int c = 0; c < CPL; ++c)
+            dst[lane + 32 * c] = make_float4(0.f, 0.f, 0.f, 0.f);
+        return;
+    }
+    // T and the flattened start of sequence b (as in fa_stream_merge_kernel)
+    long long T, P;
+    const bool scan_here = p.B <= 32 * SCAN_REG;
+    if (scan_here) {
+        int b_at;
+        long long P_at;
+        T = flat_scan(p, -1, b_at, P_at);
+        P = 0;
+        for (int b0 = 0; b0 < b; b0 += 32) {
+            const int bb = b0 + lane;
+            long long c = 0;
+            if (bb < b) {
+                int l2, h2;
+                attended_range(p, bb, l2, h2, false);
+                c = (long long)tiles_in<TILE>(l2, h2) * p.U_b;
+            }
+#pragma unroll
+            for (int off = 16; off >= 1; off >>= 1)
+                c += __shfl_xor_sync(0xffffffffu, c, off);
+            P += c;
+        }
+    } else {
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        T = p.pref[p.B];
+        P = p.pref[b];
+    }
+    const int We = workers_for(p, T);
+    const long long us = P + (long long)j * n;
+    const int wf = worker_of(us, T, We);
+    const int wl = worker_of(us + n - 1, T, We);
+    if (wf == wl)
+        return;                                   // written by the split kernel
+    if (scan_here)
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+    const long long sb = (long long)wf + (long long)b * p.U_b + j;
+    const int ns = wl - wf + 1;
+    const float2 *ml = p.ws_ml + sb * p.sh + hh;
+    const float4 *po = reinterpret_cast<const float4 *>(p.ws_o + (sb * p.sh + hh) * D) + lane;
+    const long long stride = (long long)p.sh * (D / 4);   // float4 per slot
+
+    float M = -INFINITY;
+    for (int s = lane; s < ns; s += 32)
+        M = fmaxf(M, ml[(long long)s * p.sh].x);
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1)
+        M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    float L = 0.f;
+    float4 o[CPL];
+#pragma unroll
+    for (int c = 0; c < CPL; ++c)
+        o[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s0 = 0; s0 < ns; s0 += 32) {
+        const int cnt = min(32, ns - s0);
+        const float2 v = lane < cnt ? ml[(long long)(s0 + lane) * p.sh]
+                                    : make_float2(-INFINITY, 0.f);
+        const float a = v.x == -INFINITY ? 0.f : ex2(v.x - M);
+        L = fmaf(v.y, a, L);
+#pragma unroll 8
+        for (int k = 0; k < cnt; ++k) {
+            const float ak = __shfl_sync(0xffffffffu, a, k);
+#pragma unroll
+            for (int c = 0; c < CPL; ++c) {
+                const float4 y = po[(long long)(s0 + k) * stride + 32 * c];
+                o[c].x = fmaf(y.x, ak, o[c].x);
+                o[c].y = fmaf(y.y, ak, o[c].y);
+                o[c].z = fmaf(y.z, ak, o[c].z);
+                o[c].w = fmaf(y.w, ak, o[c].w);
+            }
+        }
+    }
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1)
+        L += __shfl_xor_sync(0xffffffffu, L, off);
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+#pragma unroll
+    for (int c = 0; c < CPL; ++c)
+        dst[lane + 32 * c] = make_float4(o[c].x * inv, o[c].y * inv, o[c].z * inv, o[c].w * inv);
 }
 
 }  // namespace tc
@@ -2490,8 +2611,16 @@ static int decode_impl(const void *q, const void *k_cache, const void *v_cache,
         // programmatic dependent launch: the merge grid is scheduled while the
         // split grid drains and waits on griddepcontrol.wait for its results
         cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(batch * tq * n_q_heads);
-        cfg.blockDim = dim3(pl.path == Path::Mma ? tc::MERGE_THREADS : D / 4);
+        const long long rows = (long long)batch * tq * n_q_heads;
+        // many rows: a warp per row, eight rows per CTA (the batch-invariant
+        // plan keeps one merge form for every batch)
+        const bool by_warp = pl.path == Path::Mma && pl.chunk == 0 &&
+                             rows >= (long long)FA_MERGE_WARP_ROWS_PER_SM * sms;
+        cfg.gridDim = by_warp ? dim3(static_cast<unsigned>(
+                                    (rows + tc::MERGE_ROWS_PER_CTA - 1) / tc::MERGE_ROWS_PER_CTA))
+                              : dim3(static_cast<unsigned>(rows));
+        cfg.blockDim = dim3(by_warp ? tc::MERGE_ROWS_PER_CTA * 32
+                                    : (pl.path == Path::Mma ? tc::MERGE_THREADS : D / 4));
         cfg.dynamicSmemBytes = 0;
         cfg.stream = st;
         cudaLaunchAttribute attr[1];
@@ -2499,7 +2628,10 @@ static int decode_impl(const void *q, const void *k_cache, const void *v_cache,
         attr[0].val.programmaticStreamSerializationAllowed = prof_end ? 0 : 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        if (pl.path == Path::Mma)
+        if (by_warp)
+            e = D == 128 ? cudaLaunchKernelEx(&cfg, tc::fa_stream_merge_rows_kernel<128>, p)
+                         : cudaLaunchKernelEx(&cfg, tc::fa_stream_merge_rows_kernel<256>, p);
+        else if (pl.path == Path::Mma)
             e = pl.chunk > 0
                     ? (D == 128 ? cudaLaunchKernelEx(&cfg, tc::fa_stream_merge_kernel<128, true>, p)
                                 : cudaLaunchKernelEx(&cfg, tc::fa_stream_merge_kernel<256, true>, p))

@@ -25,6 +25,12 @@ CASES = [
     ("g4_tq4_int8_contig", 2, 8, 2, 128, 4, 0, False, True, [96, 48]),
     ("short_seqs", 3, 8, 2, 128, 6, 0, True, False, [2, 6, 1]),
     ("g1_tq8", 2, 2, 2, 128, 8, 0, True, False, [64, 1000]),
+    # 40 x 4 x 8 = 1280 output rows: at or above four rows per SM the merge
+    # takes a warp per row
+    ("many_rows_tq4", 40, 8, 2, 128, 4, 30, True, False,
+     [(i * 97) % 700 + (i % 3) for i in range(40)]),
+    ("many_rows_d256_tq3_int8", 26, 8, 2, 256, 3, 0, True, True,
+     [(i * 131) % 900 + 1 for i in range(26)]),
 ]
 
 

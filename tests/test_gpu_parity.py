@@ -291,6 +291,22 @@ def test_many_sequences_take_the_general_length_scan():
     assert_close(got, want, False, "300 sequences")
 
 
+@pytest.mark.parametrize("D,int8", [(128, False), (256, False), (256, True)])
+def test_many_rows_take_the_warp_per_row_merge(D, int8):
+    """48 sequences x 16 query heads = 768 output rows, at or above four rows
+    per SM: the merge runs a warp per row, eight rows per CTA."""
+    B = 48
+    lens = [(i * 211) % 3000 + (0 if i % 13 else 0) for i in range(B)]
+    lens[3] = 0
+    wl = W(f"many_rows_{D}_{int(int8)}", B, 16, 4, D, paged=True, v_int8=int8, window=700,
+           window_odd_only=True)
+    inp = build_case(wl, seq_lens=lens, spare_blocks=2)
+    want = oracle_decode(wl, inp)
+    got = gpu_decode(wl, to_cuda(inp)).cpu().numpy()
+    assert_close(got, want, int8, wl.name)
+    assert np.all(got[3] == 0)
+
+
 def test_one_long_unit_spans_every_worker():
     """One sequence, one KV head, one query head: the unit's partials come
     from every worker of the grid, so the merge folds more than 512 slots in
