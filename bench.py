@@ -328,7 +328,6 @@ def time_batch_invariant(wl, d, steps, warmup, device, split_tokens):
                                                          wl.head_dim, cap, split_tokens)
     ws = torch.empty(max(n, 16), dtype=torch.uint8, device=device)
     nbytes = kv_bytes(wl, d["lens"], None if d["window"] is None else d["window"].tolist())
-    flush = L2Flush(device) if nbytes < 4 * L2_BYTES else None
     stream = torch.cuda.current_stream(device)
 
     def step():
@@ -339,6 +338,15 @@ def time_batch_invariant(wl, d, steps, warmup, device, split_tokens):
             max_blocks_per_seq=d["max_blocks"], num_blocks=d["num_blocks"] if wl.paged else 0,
             workspace=ws, stream=stream)
 
+    return time_steps(step, nbytes, steps, warmup, device)
+
+
+def time_steps(step, nbytes, steps, warmup, device):
+    """Mean µs of `step()` under the headline's protocol: CUDA events on the
+    current stream, L2 flushed before every step when it reads under 4x L2."""
+    import torch
+    flush = L2Flush(device) if nbytes < 4 * L2_BYTES else None
+    stream = torch.cuda.current_stream(device)
     for i in range(warmup):
         if flush:
             flush(i)
@@ -355,6 +363,89 @@ def time_batch_invariant(wl, d, steps, warmup, device, split_tokens):
     torch.cuda.synchronize(device)
     del flush
     return 1e3 * statistics.mean(a.elapsed_time(b) for a, b in ev)
+
+
+def time_next_rows(steps, device, peak):
+    """The rows beyond the plain decode step, each timed under the headline's
+    protocol on seeded inputs of the decode shapes: ring-cache decode,
+    multi-query decode, cache append."""
+    import torch
+    from decode_step_kv_gb300 import binding
+    from decode_step_kv_gb300.inputs import WORKLOADS, kv_bytes, make_inputs, make_queries
+    stream = torch.cuda.current_stream(device)
+    res = {}
+
+    # ring cache: cfg5's heads and lengths (tokens seen ~U[128, 64K]) on a
+    # 4096-row ring per sequence, the storage of a sliding-window layer
+    C = 4096
+    wl = dataclasses.replace(WORKLOADS["cfg5"], name="ring", paged=False, window=0,
+                             window_odd_only=False)
+    d = make_inputs(wl, device, capacity=C)
+    B, Hq, Hkv, D = wl.batch, wl.n_q_heads, wl.n_kv_heads, wl.head_dim
+    nbytes = sum(min(L, C) for L in d["lens"]) * Hkv * D * 4
+    ws = binding.alloc_workspace(B, Hq, Hkv, D, C + 16, device=device)
+    out = torch.empty((B, Hq, D), dtype=torch.float32, device=device)
+    us = time_steps(lambda: binding.fa_decode_ring(
+        d["q"], d["k_cache"], d["v_cache"], None, d["seq_lens"], Hq, Hkv, D, wl.scale, None, out,
+        workspace=ws, stream=stream), nbytes, steps, 3, device)
+    gbs = nbytes / (us * 1e-6) / 1e9
+    res["ring"] = {"workload": "64 seqs, 32 q/4 kv heads, D=128, 4096-row ring per sequence, "
+                               "tokens seen ~U[128, 65536]",
+                   "us_per_step": round(us, 2), "kv_bytes": nbytes, "GB/s": round(gbs, 1),
+                   "frac_of_peak": round(gbs / peak, 4)}
+    del d, ws, out
+    torch.cuda.empty_cache()
+
+    # multi-query decode (speculative verify) on cfg3's shape: with G = 4,
+    # 2 queries make 8 (query, head) columns per KV head (one column group),
+    # 4 queries make 16 (two groups, so each K/V tile is read twice)
+    wl = WORKLOADS["cfg3"]
+    d = prepare(wl, device)
+    B, Hq, Hkv, D = wl.batch, wl.n_q_heads, wl.n_kv_heads, wl.head_dim
+    nbytes = kv_bytes(wl, d["lens"], None)
+    cap = d["max_blocks"] * wl.page_size
+    for tq in (2, 4):
+        q = make_queries(wl, tq, device)
+        n = binding.fa_decode_multi_workspace_size(B, tq, Hq, Hkv, D, cap)
+        ws = torch.empty(max(n, 16), dtype=torch.uint8, device=device)
+        out = torch.empty((B, tq, Hq, D), dtype=torch.float32, device=device)
+        us = time_steps(lambda: binding.fa_decode_multi(
+            q, d["k_cache"], d["v_cache"], None, d["block_table"], d["seq_lens"], Hq, Hkv, D,
+            wl.scale, None, out, max_blocks_per_seq=d["max_blocks"], num_blocks=d["num_blocks"],
+            workspace=ws, stream=stream), nbytes, steps, 3, device)
+        gbs = nbytes / (us * 1e-6) / 1e9
+        res[f"multi_query_tq{tq}"] = {
+            "workload": f"cfg3 shape (32 x 32K, 32 q/8 kv heads, D=128, paged), {tq} queries "
+                        "per sequence", "us_per_step": round(us, 2), "kv_bytes": nbytes,
+            "GB/s": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4),
+            "column_groups": -(-tq * wl.group // 8)}
+        del ws, out, q
+
+    # cache append: one new K/V row per (sequence, KV head) at each sequence's
+    # last position, into cfg3's paged cache (fp16 V) and cfg4's (int8 V)
+    g = torch.Generator(device=device)
+    g.manual_seed(wl.seed + 2000)
+    for name, w2 in (("append", wl), ("append_int8", WORKLOADS["cfg4"])):
+        dd = d if w2 is wl else prepare(w2, device)
+        B, Hkv, D = w2.batch, w2.n_kv_heads, w2.head_dim
+        k_new = torch.randn((B, Hkv, D), generator=g, device=device)
+        v_new = torch.randn((B, Hkv, D), generator=g, device=device)
+        pos = (dd["seq_lens"] - 1).to(torch.int32)
+        row_bytes = B * Hkv * D * (4 + (3 if w2.v_int8 else 2)) + (B * Hkv * (D // 32) * 2
+                                                                   if w2.v_int8 else 0)
+        us = time_steps(lambda: binding.fa_append_kv(
+            k_new, v_new, dd["k_cache"], dd["v_cache"], dd["v_scales"], dd["block_table"], pos,
+            n_kv_heads=Hkv, head_dim=D, page_size=w2.page_size,
+            max_blocks_per_seq=dd["max_blocks"], num_blocks=dd["num_blocks"], stream=stream),
+            row_bytes, steps, 3, device)
+        res[name] = {"workload": f"{w2.name} cache: {B} seqs x {Hkv} kv heads x D={D} rows "
+                                 f"({'int8' if w2.v_int8 else 'fp16'} V)",
+                     "us_per_call": round(us, 2)}
+        if dd is not d:
+            del dd
+    del d
+    torch.cuda.empty_cache()
+    return res
 
 
 def time_e2e(wl, d, steps, warmup, device):
@@ -588,6 +679,7 @@ def run_ours(args, world, rank, local):
             del dd
             torch.cuda.empty_cache()
         line["configs"] = per
+        line["next_rows"] = time_next_rows(max(10, min(args.steps, 30)), device, peak)
         line["batch_invariant"] = {
             "split_tokens": list(BI_SPLIT_TOKENS),
             "note": "configs[*].batch_invariant_us_per_step[split_tokens]: "

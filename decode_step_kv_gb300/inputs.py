@@ -173,6 +173,13 @@ def make_inputs(wl: Workload, device="cpu", *, seq_lens: Optional[Sequence[int]]
     return out
 
 
+def make_queries(wl: Workload, n_queries: int, device="cpu"):
+    """q [B, n_queries, Hq, D] fp16 for multi-query decode: N(0,1) rounded to
+    fp16 from its own seeded stream (seed + 1000)."""
+    g = _gen(wl.seed + 1000, torch.device(device))
+    return _normal_fp16((wl.batch, n_queries, wl.n_q_heads, wl.head_dim), g, torch.device(device))
+
+
 def attended_tokens(lens, window) -> list:
     """Per-sequence number of keys in the attended range (window applied)."""
     res = []
