@@ -102,6 +102,7 @@ struct Params {
     int sh;           // heads stored per workspace slot (stream-K)
     long long *pref;  // stream-K, more than 32*SCAN_REG sequences: [B+1] flattened
                       // start tile of each sequence (last entry: all tiles)
+    int cpu;          // tensor-core kernel: (query, head) columns per unit, 8 or 16
     int chunk;        // batch-invariant plan: tiles per chunk (0: stream-K plan)
     int max_chunks;   // batch-invariant plan: chunk slots per unit
 };
@@ -970,18 +971,19 @@ __device__ __forceinline__ int worker_of(long long t, long long T, int We)
 // normalised output (the unit lies wholly in its range) or a partial
 // (O, m, l) to workspace slot w + unit (unique: the workers covering
 // consecutive units are non-decreasing).  The merge kernel folds the slots.
-// Column c (0..7) of column group cg of KV head kv: the (query j, head h)
-// pair x = cg*8 + c = j*G + g (head-fastest); live while x < tq*G.  With one
-// query the columns are the KV head's query heads.
+// Column c (0..cpu-1) of column group cg of KV head kv, with cpu columns per
+// unit: the (query j, head h) pair x = cg*cpu + c = j*G + g (head-fastest);
+// live while x < tq*G.  With one query the columns are the KV head's query
+// heads.
 struct Col {
     bool live;
     int j;    // query index within the sequence
     int h;    // query head
 };
-__device__ __forceinline__ Col column(const Params &p, int kv, int cg, int c)
+__device__ __forceinline__ Col column(const Params &p, int kv, int cg, int c, int cpu)
 {
     const int tq = p.tq > 1 ? p.tq : 1;
-    const int x = cg * GPH + c;
+    const int x = cg * cpu + c;
     Col r;
     r.live = x < tq * p.G;
     r.j = x / p.G;
@@ -1003,8 +1005,11 @@ __device__ __forceinline__ void column_range(const Params &p, int b, int L, int 
 }
 
 // BI: the batch-invariant chunk plan instead of stream-K (a separate
-// instantiation, so the default kernel carries none of its code).
-template <int D, bool VI8, bool BI>
+// instantiation, so the default kernel carries none of its code).  NG: column
+// groups of 8 (query, head) columns a warp carries per K/V tile; 2 lets a
+// unit hold 16 columns, so more than 8 columns per KV head read each tile
+// once instead of once per group.
+template <int D, bool VI8, bool BI, int NG>
 __global__ void __launch_bounds__(Cfg<D, VI8>::NW * 32, 1)
     fa_stream_mma_kernel(const Params p, const __grid_constant__ CUtensorMap tmK,
                          const __grid_constant__ CUtensorMap tmV)
@@ -1169,50 +1174,63 @@ __global__ void __launch_bounds__(Cfg<D, VI8>::NW * 32, 1)
     }
     __syncwarp();
 
-    // Q^T of the current unit as the QK B operand: b0 = q[column g4][16ks+2t4..],
-    // b1 = +8; plus this lane's two softmax columns (2t4, 2t4+1) and their key
-    // ranges
+    // Q^T of the current unit as the QK B operand, per column group gi:
+    // b0 = q[column gi*8 + g4][16ks+2t4..], b1 = +8; plus this lane's two
+    // softmax columns (gi*8 + 2t4, +1) and their key ranges
+    constexpr int CPU = GPH * NG;          // columns per unit
     const int tq = p.tq > 1 ? p.tq : 1;
-    uint32_t qb[KS][2];
+    uint32_t qb[NG][KS][2];
     int nh = 0;                 // live columns of the unit
-    int clo0, chi0, clo1, chi1; // key ranges of columns 2t4 and 2t4+1
+    int clo[NG][2], chi[NG][2]; // key ranges of this lane's columns
     auto load_q = [&](const Walk &u) {
         const int kv = u.j / p.n_hg;
         const int cg = u.j % p.n_hg;
-        nh = min(GPH, tq * p.G - cg * GPH);
-        const Col cq = column(p, kv, cg, g4);
-        const __half *qrow = p.q + (((long long)u.b * tq + cq.j) * p.Hq + cq.h) * D;
+        nh = min(CPU, tq * p.G - cg * CPU);
 #pragma unroll
-        for (int ks = 0; ks < KS; ++ks) {
-            qb[ks][0] = cq.live ? __ldg(reinterpret_cast<const unsigned *>(qrow + ks * 16 + 2 * t4))
-                                : 0u;
-            qb[ks][1] = cq.live
-                            ? __ldg(reinterpret_cast<const unsigned *>(qrow + ks * 16 + 8 + 2 * t4))
+        for (int gi = 0; gi < NG; ++gi) {
+            const Col cq = column(p, kv, cg, gi * GPH + g4, CPU);
+            const __half *qrow = p.q + (((long long)u.b * tq + cq.j) * p.Hq + cq.h) * D;
+#pragma unroll
+            for (int ks = 0; ks < KS; ++ks) {
+                qb[gi][ks][0] =
+                    cq.live ? __ldg(reinterpret_cast<const unsigned *>(qrow + ks * 16 + 2 * t4))
                             : 0u;
+                qb[gi][ks][1] =
+                    cq.live
+                        ? __ldg(reinterpret_cast<const unsigned *>(qrow + ks * 16 + 8 + 2 * t4))
+                        : 0u;
+            }
+            const Col c0 = column(p, kv, cg, gi * GPH + 2 * t4, CPU);
+            const Col c1 = column(p, kv, cg, gi * GPH + 2 * t4 + 1, CPU);
+            column_range(p, u.b, u.hi, c0.live ? c0.j : tq - 1, clo[gi][0], chi[gi][0]);
+            column_range(p, u.b, u.hi, c1.live ? c1.j : tq - 1, clo[gi][1], chi[gi][1]);
         }
-        const Col c0 = column(p, kv, cg, 2 * t4), c1 = column(p, kv, cg, 2 * t4 + 1);
-        column_range(p, u.b, u.hi, c0.live ? c0.j : tq - 1, clo0, chi0);
-        column_range(p, u.b, u.hi, c1.live ? c1.j : tq - 1, clo1, chi1);
     };
     load_q(cw);
     // pull a unit's query rows into L2 when its first tile is issued, so the
     // switch to that unit does not wait on HBM (lane: column lane/4, line lane%4)
     auto prefetch_q = [&](const Walk &u) {
-        const Col cq = column(p, u.j / p.n_hg, u.j % p.n_hg, lane >> 2);
-        const char *base = reinterpret_cast<const char *>(
-            p.q + (((long long)u.b * tq + cq.j) * p.Hq + cq.h) * D);
-        if (cq.live && (lane & 3) * 128 < D * 2)
-            asm volatile("prefetch.global.L2 [%0];" ::"l"(base + (lane & 3) * 128));
+#pragma unroll
+        for (int gi = 0; gi < NG; ++gi) {
+            const Col cq = column(p, u.j / p.n_hg, u.j % p.n_hg, gi * GPH + (lane >> 2), CPU);
+            const char *base = reinterpret_cast<const char *>(
+                p.q + (((long long)u.b * tq + cq.j) * p.Hq + cq.h) * D);
+            if (cq.live && (lane & 3) * 128 < D * 2)
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(base + (lane & 3) * 128));
+        }
     };
 
-    float acc[KS][4];
-    float m0, m1, l0, l1;
+    float acc[NG][KS][4];
+    float m[NG][2], l[NG][2];
     auto reset = [&] {
 #pragma unroll
-        for (int i = 0; i < KS; ++i)
-            acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
-        m0 = m1 = -INFINITY;
-        l0 = l1 = 0.f;
+        for (int gi = 0; gi < NG; ++gi) {
+#pragma unroll
+            for (int i = 0; i < KS; ++i)
+                acc[gi][i][0] = acc[gi][i][1] = acc[gi][i][2] = acc[gi][i][3] = 0.f;
+            m[gi][0] = m[gi][1] = -INFINITY;
+            l[gi][0] = l[gi][1] = 0.f;
+        }
     };
     reset();
 
@@ -1296,11 +1314,17 @@ __global__ void __launch_bounds__(Cfg<D, VI8>::NW * 32, 1)
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 __syncwarp();
             }
-            // ---- S = K . Q^T  (rows: keys g4, g4+8; cols: heads 2t4, 2t4+1),
-            // even and odd k-steps in two accumulators to halve the mma chain
-            float sc4[4] = {0.f, 0.f, 0.f, 0.f};
+            // ---- S = K . Q^T per column group (rows: keys g4, g4+8; cols:
+            // 2t4, 2t4+1), even and odd k-steps in two accumulators to halve
+            // the mma chain; the K fragments serve every group
+            float sc4[NG][4];
             {
-                float sc4b[4] = {0.f, 0.f, 0.f, 0.f};
+                float sc4b[NG][4];
+#pragma unroll
+                for (int gi = 0; gi < NG; ++gi)
+#pragma unroll
+                    for (int r = 0; r < 4; ++r)
+                        sc4[gi][r] = sc4b[gi][r] = 0.f;
                 const int mi = lane >> 3;
                 const int krow = (mi & 1) * 8 + (lane & 7);
 #pragma unroll
@@ -1308,61 +1332,73 @@ __global__ void __launch_bounds__(Cfg<D, VI8>::NW * 32, 1)
                     uint32_t a0, a1, a2, a3, e0, e1, e2, e3;
                     ldsm_x4(swz(sK, krow, ks * 2 + (mi >> 1)), a0, a1, a2, a3);
                     ldsm_x4(swz(sK, krow, ks * 2 + 2 + (mi >> 1)), e0, e1, e2, e3);
-                    mma16816(sc4, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
-                    mma16816(sc4b, e0, e1, e2, e3, qb[ks + 1][0], qb[ks + 1][1]);
+#pragma unroll
+                    for (int gi = 0; gi < NG; ++gi) {
+                        mma16816(sc4[gi], a0, a1, a2, a3, qb[gi][ks][0], qb[gi][ks][1]);
+                        mma16816(sc4b[gi], e0, e1, e2, e3, qb[gi][ks + 1][0], qb[gi][ks + 1][1]);
+                    }
                 }
 #pragma unroll
-                for (int r = 0; r < 4; ++r)
-                    sc4[r] += sc4b[r];
+                for (int gi = 0; gi < NG; ++gi)
+#pragma unroll
+                    for (int r = 0; r < 4; ++r)
+                        sc4[gi][r] += sc4b[gi][r];
             }
             if constexpr (VI8 && FA_I8_INPLACE) {
                 __syncwarp();        // every lane's K reads are done: reuse the region
                 dequant_v();
             }
-            // keys outside each column's own range (tile edges, and with
-            // several queries the causal and window limits) weigh nothing
             const int ka = base + g4, kb = base + g4 + 8;
-            sc4[0] = (ka >= clo0 && ka < chi0) ? sc4[0] * p.c2 : -INFINITY;
-            sc4[1] = (ka >= clo1 && ka < chi1) ? sc4[1] * p.c2 : -INFINITY;
-            sc4[2] = (kb >= clo0 && kb < chi0) ? sc4[2] * p.c2 : -INFINITY;
-            sc4[3] = (kb >= clo1 && kb < chi1) ? sc4[3] * p.c2 : -INFINITY;
-            // ---- online softmax per head (lanes sharing t4 share the heads)
-            float x0 = fmaxf(sc4[0], sc4[2]);
-            float x1 = fmaxf(sc4[1], sc4[3]);
+            uint32_t pb0[NG], pb1[NG];
 #pragma unroll
-            for (int mask = 4; mask <= 16; mask <<= 1) {
-                x0 = fmaxf(x0, __shfl_xor_sync(0xffffffffu, x0, mask));
-                x1 = fmaxf(x1, __shfl_xor_sync(0xffffffffu, x1, mask));
-            }
-            const float n0 = fmaxf(m0, x0);
-            const float n1 = fmaxf(m1, x1);
-            // a column with no key yet keeps max -inf: use 0 as its reference
-            // so every ex2 below sees -inf (weight 0) instead of -inf - -inf
-            const float r0m = n0 == -INFINITY ? 0.f : n0;
-            const float r1m = n1 == -INFINITY ? 0.f : n1;
-            if (__any_sync(0xffffffffu, n0 > m0 || n1 > m1)) {
-                const float a0 = ex2(m0 - r0m);
-                const float a1 = ex2(m1 - r1m);
+            for (int gi = 0; gi < NG; ++gi) {
+                float *sc = sc4[gi];
+                // keys outside each column's own range (tile edges, and with
+                // several queries the causal and window limits) weigh nothing
+                sc[0] = (ka >= clo[gi][0] && ka < chi[gi][0]) ? sc[0] * p.c2 : -INFINITY;
+                sc[1] = (ka >= clo[gi][1] && ka < chi[gi][1]) ? sc[1] * p.c2 : -INFINITY;
+                sc[2] = (kb >= clo[gi][0] && kb < chi[gi][0]) ? sc[2] * p.c2 : -INFINITY;
+                sc[3] = (kb >= clo[gi][1] && kb < chi[gi][1]) ? sc[3] * p.c2 : -INFINITY;
+                // ---- online softmax per column (lanes sharing t4 share them)
+                float x0 = fmaxf(sc[0], sc[2]);
+                float x1 = fmaxf(sc[1], sc[3]);
 #pragma unroll
-                for (int ii = 0; ii < KS; ++ii) {
-                    acc[ii][0] *= a0;
-                    acc[ii][1] *= a1;
-                    acc[ii][2] *= a0;
-                    acc[ii][3] *= a1;
+                for (int mask = 4; mask <= 16; mask <<= 1) {
+                    x0 = fmaxf(x0, __shfl_xor_sync(0xffffffffu, x0, mask));
+                    x1 = fmaxf(x1, __shfl_xor_sync(0xffffffffu, x1, mask));
                 }
-                l0 *= a0;
-                l1 *= a1;
-                m0 = n0;
-                m1 = n1;
+                const float n0 = fmaxf(m[gi][0], x0);
+                const float n1 = fmaxf(m[gi][1], x1);
+                // a column with no key yet keeps max -inf: use 0 as its
+                // reference so every ex2 below sees -inf (weight 0) instead
+                // of -inf - -inf
+                const float r0m = n0 == -INFINITY ? 0.f : n0;
+                const float r1m = n1 == -INFINITY ? 0.f : n1;
+                if (__any_sync(0xffffffffu, n0 > m[gi][0] || n1 > m[gi][1])) {
+                    const float a0 = ex2(m[gi][0] - r0m);
+                    const float a1 = ex2(m[gi][1] - r1m);
+#pragma unroll
+                    for (int ii = 0; ii < KS; ++ii) {
+                        acc[gi][ii][0] *= a0;
+                        acc[gi][ii][1] *= a1;
+                        acc[gi][ii][2] *= a0;
+                        acc[gi][ii][3] *= a1;
+                    }
+                    l[gi][0] *= a0;
+                    l[gi][1] *= a1;
+                    m[gi][0] = n0;
+                    m[gi][1] = n1;
+                }
+                const float p0 = ex2(sc[0] - r0m), p1 = ex2(sc[1] - r1m);
+                const float p2 = ex2(sc[2] - r0m), p3 = ex2(sc[3] - r1m);
+                l[gi][0] += p0 + p2;
+                l[gi][1] += p1 + p3;
+                // ---- P^T as the PV B operand (keys x columns), via movmatrix
+                pb0[gi] = movmatrix_t(pack_half2(p0, p1));
+                pb1[gi] = movmatrix_t(pack_half2(p2, p3));
             }
-            const float p0 = ex2(sc4[0] - r0m), p1 = ex2(sc4[1] - r1m);
-            const float p2 = ex2(sc4[2] - r0m), p3 = ex2(sc4[3] - r1m);
-            l0 += p0 + p2;
-            l1 += p1 + p3;
-            // ---- P^T as the PV B operand (keys x heads), via movmatrix
-            const uint32_t pb0 = movmatrix_t(pack_half2(p0, p1));
-            const uint32_t pb1 = movmatrix_t(pack_half2(p2, p3));
-            // ---- O^T += V^T . P^T  (rows: head_dim; cols: heads)
+            // ---- O^T += V^T . P^T  (rows: head_dim; cols: columns); the V
+            // fragments serve every group
             {
                 const int mi = lane >> 3;
                 const int vrow = (mi >> 1) * 8 + (lane & 7);
@@ -1370,7 +1406,9 @@ __global__ void __launch_bounds__(Cfg<D, VI8>::NW * 32, 1)
                 for (int mt = 0; mt < KS; ++mt) {
                     uint32_t a0, a1, a2, a3;
                     ldsm_x4_t(swz(sV, vrow, mt * 2 + (mi & 1)), a0, a1, a2, a3);
-                    mma16816(acc[mt], a0, a1, a2, a3, pb0, pb1);
+#pragma unroll
+                    for (int gi = 0; gi < NG; ++gi)
+                        mma16816(acc[gi][mt], a0, a1, a2, a3, pb0[gi], pb1[gi]);
                 }
             }
         }
@@ -1391,10 +1429,12 @@ __global__ void __launch_bounds__(Cfg<D, VI8>::NW * 32, 1)
             // ---- end of this worker's segment of the unit (with the
             // batch-invariant plan: of a chunk): publish it
 #pragma unroll
-            for (int mask = 4; mask <= 16; mask <<= 1) {
-                l0 += __shfl_xor_sync(0xffffffffu, l0, mask);
-                l1 += __shfl_xor_sync(0xffffffffu, l1, mask);
-            }
+            for (int gi = 0; gi < NG; ++gi)
+#pragma unroll
+                for (int mask = 4; mask <= 16; mask <<= 1) {
+                    l[gi][0] += __shfl_xor_sync(0xffffffffu, l[gi][0], mask);
+                    l[gi][1] += __shfl_xor_sync(0xffffffffu, l[gi][1], mask);
+                }
             bool whole;          // the segment is the whole unit: normalised output
             long long slot;      // else its partial's workspace slot
             if constexpr (BI) {
@@ -1408,45 +1448,48 @@ __global__ void __launch_bounds__(Cfg<D, VI8>::NW * 32, 1)
                 slot = w + cw.unit(p);
             }
             const int kvu = cw.j / p.n_hg, cgu = cw.j % p.n_hg;
-            const int h0 = 2 * t4, h1 = 2 * t4 + 1;   // this lane's columns
-            const Col c0 = column(p, kvu, cgu, h0), c1 = column(p, kvu, cgu, h1);
-            if (whole) {
-                // the whole unit was ours: normalised output
-                const float i0 = l0 > 0.f ? 1.f / l0 : 0.f;
-                const float i1 = l1 > 0.f ? 1.f / l1 : 0.f;
-                float *o0 = p.out + (((long long)cw.b * tq + c0.j) * p.Hq + c0.h) * D;
-                float *o1 = p.out + (((long long)cw.b * tq + c1.j) * p.Hq + c1.h) * D;
 #pragma unroll
-                for (int mt = 0; mt < KS; ++mt) {
-                    const int d = mt * 16 + g4;
-                    if (c0.live) {
-                        o0[d] = acc[mt][0] * i0;
-                        o0[d + 8] = acc[mt][2] * i0;
-                    }
-                    if (c1.live) {
-                        o1[d] = acc[mt][1] * i1;
-                        o1[d + 8] = acc[mt][3] * i1;
-                    }
-                }
-            } else {
-                float *o = p.ws_o + slot * p.sh * D;
+            for (int gi = 0; gi < NG; ++gi) {
+                const int h0 = gi * GPH + 2 * t4, h1 = h0 + 1;   // this lane's columns
+                const Col c0 = column(p, kvu, cgu, h0, CPU), c1 = column(p, kvu, cgu, h1, CPU);
+                if (whole) {
+                    // the whole unit was ours: normalised output
+                    const float i0 = l[gi][0] > 0.f ? 1.f / l[gi][0] : 0.f;
+                    const float i1 = l[gi][1] > 0.f ? 1.f / l[gi][1] : 0.f;
+                    float *o0 = p.out + (((long long)cw.b * tq + c0.j) * p.Hq + c0.h) * D;
+                    float *o1 = p.out + (((long long)cw.b * tq + c1.j) * p.Hq + c1.h) * D;
 #pragma unroll
-                for (int mt = 0; mt < KS; ++mt) {
-                    const int d = mt * 16 + g4;
-                    if (h0 < nh) {
-                        o[h0 * D + d] = acc[mt][0];
-                        o[h0 * D + d + 8] = acc[mt][2];
+                    for (int mt = 0; mt < KS; ++mt) {
+                        const int d = mt * 16 + g4;
+                        if (c0.live) {
+                            o0[d] = acc[gi][mt][0] * i0;
+                            o0[d + 8] = acc[gi][mt][2] * i0;
+                        }
+                        if (c1.live) {
+                            o1[d] = acc[gi][mt][1] * i1;
+                            o1[d + 8] = acc[gi][mt][3] * i1;
+                        }
                     }
-                    if (h1 < nh) {
-                        o[h1 * D + d] = acc[mt][1];
-                        o[h1 * D + d + 8] = acc[mt][3];
+                } else {
+                    float *o = p.ws_o + slot * p.sh * D;
+#pragma unroll
+                    for (int mt = 0; mt < KS; ++mt) {
+                        const int d = mt * 16 + g4;
+                        if (h0 < nh) {
+                            o[h0 * D + d] = acc[gi][mt][0];
+                            o[h0 * D + d + 8] = acc[gi][mt][2];
+                        }
+                        if (h1 < nh) {
+                            o[h1 * D + d] = acc[gi][mt][1];
+                            o[h1 * D + d + 8] = acc[gi][mt][3];
+                        }
                     }
-                }
-                if (g4 == 0) {
-                    if (h0 < nh)
-                        p.ws_ml[slot * p.sh + h0] = make_float2(m0, l0);
-                    if (h1 < nh)
-                        p.ws_ml[slot * p.sh + h1] = make_float2(m1, l1);
+                    if (g4 == 0) {
+                        if (h0 < nh)
+                            p.ws_ml[slot * p.sh + h0] = make_float2(m[gi][0], l[gi][0]);
+                        if (h1 < nh)
+                            p.ws_ml[slot * p.sh + h1] = make_float2(m[gi][1], l[gi][1]);
+                    }
                 }
             }
             reset();
@@ -1504,8 +1547,8 @@ __global__ void __launch_bounds__(MERGE_THREADS) fa_stream_merge_kernel(const Pa
     const int h = static_cast<int>(row % p.Hq);
     const int kv = h / p.G;
     const int x = qj * p.G + h % p.G;
-    const int j = kv * p.n_hg + x / GPH;
-    const int hh = x % GPH;
+    const int j = kv * p.n_hg + x / p.cpu;
+    const int hh = x % p.cpu;
     const int tid = threadIdx.x;
     const int lane = tid & 31, wid = tid >> 5;
 
@@ -1707,8 +1750,8 @@ __global__ void __launch_bounds__(MERGE_ROWS_PER_CTA * 32) fa_stream_merge_rows_
     const int h = static_cast<int>(row % p.Hq);
     const int kv = h / p.G;
     const int x = qj * p.G + h % p.G;
-    const int j = kv * p.n_hg + x / GPH;
-    const int hh = x % GPH;
+    const int j = kv * p.n_hg + x / p.cpu;
+    const int hh = x % p.cpu;
     float4 *dst = reinterpret_cast<float4 *>(p.out + row * D);
 
     int lo, hi;
@@ -2000,6 +2043,7 @@ struct Plan {
     int max_splits;
     int chunk;       // batch-invariant plan: tiles per chunk (0: stream-K)
     int max_chunks;  // batch-invariant plan: chunk slots per unit
+    int cpu;         // tensor-core kernel: columns per unit (8, or 16: two groups per warp)
 };
 
 static int next_pow2(int x)
@@ -2036,9 +2080,13 @@ static Plan make_plan(Path path, int B, int Hq, int Hkv, int D, long long cap, i
         pl.tile = tc::TILE;
         pl.gp = tc::GPH;
         pl.hpg = tc::GPH;
-        // columns: the (query, head) pairs of one KV head, in groups of 8
-        pl.n_hg = (tq * G + tc::GPH - 1) / tc::GPH;
-        pl.sh = tq * G < tc::GPH ? tq * G : tc::GPH;
+        // columns: the (query, head) pairs of one KV head, in units of 8, or
+        // of 16 at D=128 when there are more than 8 (a warp then carries two
+        // groups, reading each K/V tile once for both; the batch-invariant
+        // plan keeps 8)
+        pl.cpu = (D == 128 && chunk == 0 && tq * G > tc::GPH) ? 2 * tc::GPH : tc::GPH;
+        pl.n_hg = (tq * G + pl.cpu - 1) / pl.cpu;
+        pl.sh = tq * G < pl.cpu ? tq * G : pl.cpu;
         pl.units = Hkv * pl.n_hg;
         int nw, cps;
         if (D == 128) {
@@ -2213,7 +2261,7 @@ static int encode_kv_map(CUtensorMap *map, const void *base, long long rows, int
     return 0;
 }
 
-template <int D, bool VI8, bool BI>
+template <int D, bool VI8, bool BI, int NG = 1>
 static cudaError_t launch_mma(const Params &p, const CUtensorMap &tmK, const CUtensorMap &tmV,
                               dim3 grid, cudaStream_t st)
 {
@@ -2227,7 +2275,7 @@ static cudaError_t launch_mma(const Params &p, const CUtensorMap &tmK, const CUt
     {
         std::lock_guard<std::mutex> lock(mu);
         if (dev >= 64 || !done[dev]) {
-            e = cudaFuncSetAttribute(tc::fa_stream_mma_kernel<D, VI8, BI>,
+            e = cudaFuncSetAttribute(tc::fa_stream_mma_kernel<D, VI8, BI, NG>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
             if (e != cudaSuccess)
                 return e;
@@ -2235,8 +2283,8 @@ static cudaError_t launch_mma(const Params &p, const CUtensorMap &tmK, const CUt
                 done[dev] = true;
         }
     }
-    tc::fa_stream_mma_kernel<D, VI8, BI><<<grid, tc::Cfg<D, VI8>::NW * 32, smem, st>>>(p, tmK,
-                                                                                     tmV);
+    tc::fa_stream_mma_kernel<D, VI8, BI, NG><<<grid, tc::Cfg<D, VI8>::NW * 32, smem, st>>>(
+        p, tmK, tmV);
     return cudaGetLastError();
 }
 
@@ -2560,6 +2608,7 @@ static int decode_impl(const void *q, const void *k_cache, const void *v_cache,
     p.sh = pl.sh;
     p.chunk = pl.chunk;
     p.max_chunks = pl.max_chunks;
+    p.cpu = pl.cpu;
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const dim3 grid = pl.path == Path::Mma ? dim3(pl.ctas)
@@ -2581,6 +2630,8 @@ static int decode_impl(const void *q, const void *k_cache, const void *v_cache,
             if (pl.chunk > 0)
                 e = D == 128 ? launch_mma<128, true, true>(p, tmK, tmV, grid, st)
                              : launch_mma<256, true, true>(p, tmK, tmV, grid, st);
+            else if (pl.cpu > tc::GPH)
+                e = launch_mma<128, true, false, 2>(p, tmK, tmV, grid, st);   // D = 128 only
             else
                 e = D == 128 ? launch_mma<128, true, false>(p, tmK, tmV, grid, st)
                              : launch_mma<256, true, false>(p, tmK, tmV, grid, st);
@@ -2591,6 +2642,8 @@ static int decode_impl(const void *q, const void *k_cache, const void *v_cache,
             if (pl.chunk > 0)
                 e = D == 128 ? launch_mma<128, false, true>(p, tmK, tmV, grid, st)
                              : launch_mma<256, false, true>(p, tmK, tmV, grid, st);
+            else if (pl.cpu > tc::GPH)
+                e = launch_mma<128, false, false, 2>(p, tmK, tmV, grid, st);  // D = 128 only
             else
                 e = D == 128 ? launch_mma<128, false, false>(p, tmK, tmV, grid, st)
                              : launch_mma<256, false, false>(p, tmK, tmV, grid, st);
