@@ -1,0 +1,113 @@
+"""Parity at the sizes the benchmark times for the rows beyond the plain
+decode step: multi-query decode (4 queries) and the batch-invariant plan on
+the 32 x 32K, 32/8-head, D=128 paged workload, and ring decode on 64
+sequences with cfg5's heads and lengths over 4096-row rings.  The oracle
+recomputes a sample of the sequences (every output row of each), each from a
+host copy of that sequence's cache alone.
+"""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from decode_step_kv_gb300 import binding
+from decode_step_kv_gb300.inputs import WORKLOADS, make_inputs, make_queries
+
+from _helpers import assert_close
+
+pytestmark = pytest.mark.gpu
+
+
+def _sample(B, n=4, seed=0):
+    rng = np.random.default_rng(seed)
+    return sorted(set([0, B - 1] + [int(x) for x in rng.choice(B, n, replace=False)]))
+
+
+def _seq_blocks(d, b, P):
+    """Sequence b's K/V blocks on the host, with an identity block table."""
+    L = d["lens"][b]
+    nb = -(-L // P)
+    sel = d["block_table"][b, :nb].long()
+    k = d["k_cache"].index_select(0, sel).cpu().numpy()
+    v = d["v_cache"].index_select(0, sel).cpu().numpy()
+    return L, nb, k, v, np.arange(nb, dtype=np.int32)[None, :]
+
+
+@pytest.fixture(scope="module")
+def cfg3():
+    wl = WORKLOADS["cfg3"]
+    torch.cuda.empty_cache()
+    d = make_inputs(wl, "cuda")
+    yield wl, d
+    del d
+    torch.cuda.empty_cache()
+
+
+def test_multi_query_four_queries_at_full_size(cfg3):
+    """16 (query, head) columns per KV head: the two-column-group kernel."""
+    wl, d = cfg3
+    tq = 4
+    B, Hq, Hkv, D = wl.batch, wl.n_q_heads, wl.n_kv_heads, wl.head_dim
+    q = make_queries(wl, tq, "cuda")
+    cap = d["max_blocks"] * wl.page_size
+    n = binding.fa_decode_multi_workspace_size(B, tq, Hq, Hkv, D, cap)
+    ws = torch.full((max(n, 16),), 0xFF, dtype=torch.uint8, device="cuda")
+    out = torch.full((B, tq, Hq, D), float("nan"), device="cuda")
+    binding.fa_decode_multi(q, d["k_cache"], d["v_cache"], None, d["block_table"],
+                            d["seq_lens"], Hq, Hkv, D, wl.scale, None, out,
+                            max_blocks_per_seq=d["max_blocks"], num_blocks=d["num_blocks"],
+                            workspace=ws)
+    got = out.cpu().numpy()
+    assert np.all(np.isfinite(got))
+    for b in _sample(B, n=2):
+        L, nb, k, v, bt = _seq_blocks(d, b, wl.page_size)
+        want = oracle.decode_multi(q[b:b + 1].cpu().numpy(), k, v, [L], scale=wl.scale,
+                                   n_kv_heads=Hkv, block_table=bt, page_size=wl.page_size,
+                                   max_blocks=nb)
+        assert_close(got[b:b + 1], want, False, f"multi-query sequence {b}")
+
+
+def test_batch_invariant_1024_at_full_size(cfg3):
+    wl, d = cfg3
+    B, Hq, Hkv, D = wl.batch, wl.n_q_heads, wl.n_kv_heads, wl.head_dim
+    cap = d["max_blocks"] * wl.page_size
+    n = binding.fa_decode_batch_invariant_workspace_size(B, Hq, Hkv, D, cap, 1024)
+    ws = torch.full((max(n, 16),), 0xFF, dtype=torch.uint8, device="cuda")
+    out = torch.full((B, Hq, D), float("nan"), device="cuda")
+    binding.fa_decode_batch_invariant(d["q"], d["k_cache"], d["v_cache"], None,
+                                      d["block_table"], d["seq_lens"], Hq, Hkv, D, wl.scale, None,
+                                      out, split_tokens=1024, workspace=ws)
+    got = out.cpu().numpy()
+    assert np.all(np.isfinite(got))
+    for b in _sample(B, n=2, seed=1):
+        L, nb, k, v, bt = _seq_blocks(d, b, wl.page_size)
+        want = oracle.decode(d["q"][b:b + 1].cpu().numpy(), k, v, [L], scale=wl.scale,
+                             n_kv_heads=Hkv, block_table=bt, page_size=wl.page_size,
+                             max_blocks=nb)
+        assert_close(got[b:b + 1], want, False, f"batch-invariant sequence {b}")
+
+
+def test_ring_decode_at_bench_size():
+    C = 4096
+    wl = dataclasses.replace(WORKLOADS["cfg5"], name="ring", paged=False, window=0,
+                             window_odd_only=False)
+    torch.cuda.empty_cache()
+    d = make_inputs(wl, "cuda", capacity=C)
+    B, Hq, Hkv, D = wl.batch, wl.n_q_heads, wl.n_kv_heads, wl.head_dim
+    ws = binding.alloc_workspace(B, Hq, Hkv, D, C + 16)
+    ws.fill_(0xFF)
+    out = torch.full((B, Hq, D), float("nan"), device="cuda")
+    binding.fa_decode_ring(d["q"], d["k_cache"], d["v_cache"], None, d["seq_lens"], Hq, Hkv, D,
+                           wl.scale, None, out, workspace=ws)
+    got = out.cpu().numpy()
+    assert np.all(np.isfinite(got))
+    for b in _sample(B, n=4, seed=2):
+        want = oracle.decode_ring(d["q"][b:b + 1].cpu().numpy(),
+                                  d["k_cache"][b:b + 1].cpu().numpy(),
+                                  d["v_cache"][b:b + 1].cpu().numpy(), [d["lens"][b]],
+                                  scale=wl.scale, n_kv_heads=Hkv)
+        assert_close(got[b:b + 1], want, False, f"ring sequence {b} ({d['lens'][b]} tokens)")
+    del d
+    torch.cuda.empty_cache()
