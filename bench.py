@@ -421,6 +421,29 @@ def time_next_rows(steps, device, peak):
             "column_groups": -(-tq * wl.group // 8)}
         del ws, out, q
 
+    # multi-query decode at D=256: cfg4's shape with fp16 V and 8 queries (16
+    # columns per KV head: two groups per warp, the query rows in shared memory)
+    wl2 = dataclasses.replace(WORKLOADS["cfg4"], name="cfg4_fp16", v_int8=False)
+    d2 = prepare(wl2, device)
+    B2, Hq2, Hkv2, D2 = wl2.batch, wl2.n_q_heads, wl2.n_kv_heads, wl2.head_dim
+    nbytes2 = kv_bytes(wl2, d2["lens"], None)
+    q = make_queries(wl2, 8, device)
+    n = binding.fa_decode_multi_workspace_size(B2, 8, Hq2, Hkv2, D2,
+                                               d2["max_blocks"] * wl2.page_size)
+    ws = torch.empty(max(n, 16), dtype=torch.uint8, device=device)
+    out = torch.empty((B2, 8, Hq2, D2), dtype=torch.float32, device=device)
+    us = time_steps(lambda: binding.fa_decode_multi(
+        q, d2["k_cache"], d2["v_cache"], None, d2["block_table"], d2["seq_lens"], Hq2, Hkv2, D2,
+        wl2.scale, None, out, max_blocks_per_seq=d2["max_blocks"], num_blocks=d2["num_blocks"],
+        workspace=ws, stream=stream), nbytes2, steps, 3, device)
+    gbs = nbytes2 / (us * 1e-6) / 1e9
+    res["multi_query_d256_tq8"] = {
+        "workload": "16 x 16K, 16 q/8 kv heads, D=256, paged, fp16 V (cfg4 with fp16 V), "
+                    "8 queries per sequence", "us_per_step": round(us, 2), "kv_bytes": nbytes2,
+        "GB/s": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4), "column_groups": 2}
+    del d2, q, ws, out
+    torch.cuda.empty_cache()
+
     # cache append: one new K/V row per (sequence, KV head) at each sequence's
     # last position, into cfg3's paged cache (fp16 V) and cfg4's (int8 V)
     g = torch.Generator(device=device)

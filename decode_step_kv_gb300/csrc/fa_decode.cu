@@ -699,6 +699,22 @@ struct Cfg {
     static_assert(CTAS_PER_SM * (SMEM + 1024) <= 228 * 1024, "shared memory per SM");
 };
 
+// Shared memory of the stream-K kernel: the rings and barriers, plus, when
+// two column groups ride a warp at D=256 (QSM), each warp's 16 query rows,
+// kept there instead of in registers (with int8 V at D=256 they do not fit,
+// so that kernel keeps one group).
+template <int D, bool VI8, int NG>
+struct Smem {
+    static constexpr bool QSM = D == 256 && NG == 2;
+    static constexpr int Q_OFF = Cfg<D, VI8>::RING_BYTES + 1024;   // after the barriers
+    static constexpr int Q_WARP = 2 * GPH * D * 2;                   // 16 rows x D fp16
+    static constexpr int BYTES =
+        QSM ? Q_OFF + Cfg<D, VI8>::NW * Q_WARP + 1024 : Cfg<D, VI8>::SMEM;
+    static_assert(Cfg<D, VI8>::NW * Cfg<D, VI8>::STAGES * 8 <= 1024, "barriers before Q_OFF");
+    static_assert(Cfg<D, VI8>::CTAS_PER_SM * (BYTES + 1024) <= 228 * 1024,
+                  "shared memory per SM");
+};
+
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y,
                                             uint32_t bar, uint64_t policy)
 {
@@ -1131,6 +1147,9 @@ __global__ void __launch_bounds__(Cfg<D, VI8>::NW * 32, 1)
     const uint32_t ring = smem_u32(smem) + warp * C::WARP_BYTES;
     const uint32_t cvt = ring + STAGES * C::STAGE_BYTES;     // int8 V: dequantised tile
     const uint32_t my_bars = smem_u32(bars + warp * STAGES);
+    using SM = Smem<D, VI8, NG>;
+    constexpr bool QSM = SM::QSM;
+    const uint32_t qs = smem_u32(smem) + SM::Q_OFF + warp * SM::Q_WARP;   // QSM: query rows
 
     if (lane == 0)
         for (int s = 0; s < STAGES; ++s)
@@ -1182,26 +1201,46 @@ __global__ void __launch_bounds__(Cfg<D, VI8>::NW * 32, 1)
     // softmax columns (gi*8 + 2t4, +1) and their key ranges
     constexpr int CPU = GPH * NG;          // columns per unit
     const int tq = p.tq > 1 ? p.tq : 1;
-    uint32_t qb[NG][KS][2];
+    uint32_t qb[QSM ? 1 : NG][KS][2];
     int nh = 0;                 // live columns of the unit
     int clo[NG][2], chi[NG][2]; // key ranges of this lane's columns
     auto load_q = [&](const Walk &u) {
         const int kv = u.j / p.n_hg;
         const int cg = u.j % p.n_hg;
         nh = min(CPU, tq * p.G - cg * CPU);
+        if constexpr (QSM) {
+            // the unit's CPU query rows in 16-byte chunks, chunk index
+            // XOR-ed with the row so that ldmatrix's 8-row reads hit 8 banks
+            constexpr int CH16 = D / 8;
+            for (int idx = lane; idx < CPU * CH16; idx += 32) {
+                const int r = idx / CH16, ch = idx % CH16;
+                const Col cq = column(p, kv, cg, r, CPU);
+                uint4 v = make_uint4(0u, 0u, 0u, 0u);
+                if (cq.live)
+                    v = __ldg(reinterpret_cast<const uint4 *>(
+                                  p.q + (((long long)u.b * tq + cq.j) * p.Hq + cq.h) * D) +
+                              ch);
+                asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(
+                                 qs + r * (D * 2) + ((ch ^ (r & 7)) * 16)),
+                             "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                             : "memory");
+            }
+            __syncwarp();
+        }
 #pragma unroll
         for (int gi = 0; gi < NG; ++gi) {
-            const Col cq = column(p, kv, cg, gi * GPH + g4, CPU);
-            const __half *qrow = p.q + (((long long)u.b * tq + cq.j) * p.Hq + cq.h) * D;
+            if constexpr (!QSM) {
+                const Col cq = column(p, kv, cg, gi * GPH + g4, CPU);
+                const __half *qrow = p.q + (((long long)u.b * tq + cq.j) * p.Hq + cq.h) * D;
 #pragma unroll
-            for (int ks = 0; ks < KS; ++ks) {
-                qb[gi][ks][0] =
-                    cq.live ? __ldg(reinterpret_cast<const unsigned *>(qrow + ks * 16 + 2 * t4))
-                            : 0u;
-                qb[gi][ks][1] =
-                    cq.live
-                        ? __ldg(reinterpret_cast<const unsigned *>(qrow + ks * 16 + 8 + 2 * t4))
-                        : 0u;
+                for (int ks = 0; ks < KS; ++ks) {
+                    qb[gi][ks][0] = cq.live ? __ldg(reinterpret_cast<const unsigned *>(
+                                                  qrow + ks * 16 + 2 * t4))
+                                            : 0u;
+                    qb[gi][ks][1] = cq.live ? __ldg(reinterpret_cast<const unsigned *>(
+                                                  qrow + ks * 16 + 8 + 2 * t4))
+                                            : 0u;
+                }
             }
             const Col c0 = column(p, kv, cg, gi * GPH + 2 * t4, CPU);
             const Col c1 = column(p, kv, cg, gi * GPH + 2 * t4 + 1, CPU);
@@ -1337,8 +1376,21 @@ __global__ void __launch_bounds__(Cfg<D, VI8>::NW * 32, 1)
                     ldsm_x4(swz(sK, krow, ks * 2 + 2 + (mi >> 1)), e0, e1, e2, e3);
 #pragma unroll
                     for (int gi = 0; gi < NG; ++gi) {
-                        mma16816(sc4[gi], a0, a1, a2, a3, qb[gi][ks][0], qb[gi][ks][1]);
-                        mma16816(sc4b[gi], e0, e1, e2, e3, qb[gi][ks + 1][0], qb[gi][ks + 1][1]);
+                        uint32_t b0, b1, c0, c1;
+                        if constexpr (QSM) {
+                            // rows gi*8 + 0..7, chunks 2ks .. 2ks+3: the B
+                            // fragments of k-steps ks and ks+1
+                            const int row = gi * GPH + (lane & 7);
+                            const int ch = 2 * ks + (lane >> 3);
+                            ldsm_x4(qs + row * (D * 2) + ((ch ^ (row & 7)) * 16), b0, b1, c0, c1);
+                        } else {
+                            b0 = qb[gi][ks][0];
+                            b1 = qb[gi][ks][1];
+                            c0 = qb[gi][ks + 1][0];
+                            c1 = qb[gi][ks + 1][1];
+                        }
+                        mma16816(sc4[gi], a0, a1, a2, a3, b0, b1);
+                        mma16816(sc4b[gi], e0, e1, e2, e3, c0, c1);
                     }
                 }
 #pragma unroll
@@ -2072,6 +2124,10 @@ static Path choose_path()
 // Split planner: sizes splits from batch x kv_heads x capacity so that the
 // grid holds several waves of resident CTAs (the "nwg" of the pages, chosen
 // here from the SM count rather than a fixed bucket).
+// K/V bytes (at full capacity) from which units of 16 columns are used: four
+// times GB300's 126.5 MiB L2.
+constexpr double TWO_GROUP_MIN_KV_BYTES = 512.0 * (1 << 20);
+
 static Plan make_plan(Path path, int B, int Hq, int Hkv, int D, long long cap, int num_sms,
                       bool vi8, int tq = 1, int chunk = 0)
 {
@@ -2084,10 +2140,19 @@ static Plan make_plan(Path path, int B, int Hq, int Hkv, int D, long long cap, i
         pl.gp = tc::GPH;
         pl.hpg = tc::GPH;
         // columns: the (query, head) pairs of one KV head, in units of 8, or
-        // of 16 at D=128 when there are more than 8 (a warp then carries two
-        // groups, reading each K/V tile once for both; the batch-invariant
-        // plan keeps 8)
-        pl.cpu = (D == 128 && chunk == 0 && tq * G > tc::GPH) ? 2 * tc::GPH : tc::GPH;
+        // of 16 when there are more than 8 (a warp then carries two groups,
+        // reading each K/V tile once for both).  Two groups pay off when the
+        // step streams from HBM; on a step whose K/V fits in L2 the second
+        // group's re-read hits L2 and the single-group units keep twice the
+        // warps busy, so the choice goes by the K/V the capacity allows.
+        // int8 V at D=256 has no room for two groups; the batch-invariant
+        // plan keeps 8.
+        const double kv_bound = (double)B * (double)cap * Hkv *
+                                (2.0 * D + (vi8 ? D + D / 16.0 : 2.0 * D));
+        pl.cpu = ((D == 128 || !vi8) && chunk == 0 && tq * G > tc::GPH &&
+                  kv_bound >= TWO_GROUP_MIN_KV_BYTES)
+                     ? 2 * tc::GPH
+                     : tc::GPH;
         pl.n_hg = (tq * G + pl.cpu - 1) / pl.cpu;
         pl.sh = tq * G < pl.cpu ? tq * G : pl.cpu;
         pl.units = Hkv * pl.n_hg;
@@ -2268,7 +2333,7 @@ template <int D, bool VI8, bool BI, int NG = 1>
 static cudaError_t launch_mma(const Params &p, const CUtensorMap &tmK, const CUtensorMap &tmV,
                               dim3 grid, cudaStream_t st)
 {
-    const int smem = tc::Cfg<D, VI8>::SMEM;
+    const int smem = tc::Smem<D, VI8, NG>::BYTES;
     static std::mutex mu;
     static bool done[64] = {false};
     int dev = 0;
@@ -2646,7 +2711,8 @@ static int decode_impl(const void *q, const void *k_cache, const void *v_cache,
                 e = D == 128 ? launch_mma<128, false, true>(p, tmK, tmV, grid, st)
                              : launch_mma<256, false, true>(p, tmK, tmV, grid, st);
             else if (pl.cpu > tc::GPH)
-                e = launch_mma<128, false, false, 2>(p, tmK, tmV, grid, st);  // D = 128 only
+                e = D == 128 ? launch_mma<128, false, false, 2>(p, tmK, tmV, grid, st)
+                             : launch_mma<256, false, false, 2>(p, tmK, tmV, grid, st);
             else
                 e = D == 128 ? launch_mma<128, false, false>(p, tmK, tmV, grid, st)
                              : launch_mma<256, false, false>(p, tmK, tmV, grid, st);

@@ -25,6 +25,9 @@ CASES = [
     ("g4_tq4_int8_contig", 2, 8, 2, 128, 4, 0, False, True, [96, 48]),
     ("short_seqs", 3, 8, 2, 128, 6, 0, True, False, [2, 6, 1]),
     ("g1_tq8", 2, 2, 2, 128, 8, 0, True, False, [64, 1000]),
+    ("g2_d256_tq8", 3, 4, 2, 256, 8, 0, True, False, [900, 2000, 5]),
+    ("g2_d256_tq6_window_contig", 2, 4, 2, 256, 6, 50, False, False, [300, 64]),
+    ("g4_d256_tq7_ragged", 5, 8, 2, 256, 7, 0, True, False, [1, 7, 33, 1500, 4000]),
     # 40 x 4 x 8 = 1280 output rows: at or above four rows per SM the merge
     # takes a warp per row
     ("many_rows_tq4", 40, 8, 2, 128, 4, 30, True, False,
@@ -33,13 +36,30 @@ CASES = [
      [(i * 131) % 900 + 1 for i in range(26)]),
 ]
 
+# The same kind of cases with a block table of 2^20 tokens per sequence: the
+# K/V the capacity allows passes the two-column-group threshold, so units
+# hold 16 columns (at D=256 with the query rows in shared memory), while the
+# pool holds only the blocks the lengths need.
+BIG_CAP = 1 << 20
+CASES_TWO_GROUPS = [
+    ("2g_g4_tq4_window", 3, 8, 2, 128, 4, 5, True, False, [100, 1000, 40]),
+    ("2g_g8_tq3", 2, 16, 2, 128, 3, 0, True, False, [500, 33]),
+    ("2g_g4_tq4_int8", 3, 8, 2, 128, 4, 0, True, True, [96, 1500, 7]),
+    ("2g_d256_tq8", 3, 4, 2, 256, 8, 0, True, False, [900, 2000, 5]),
+    ("2g_d256_tq6_window", 2, 4, 2, 256, 6, 50, True, False, [300, 64]),
+    ("2g_d256_tq7_ragged", 5, 8, 2, 256, 7, 0, True, False, [1, 7, 33, 1500, 4000]),
+]
 
-@pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
+
+ALL_CASES = [c + (None,) for c in CASES] + [c + (BIG_CAP,) for c in CASES_TWO_GROUPS]
+
+
+@pytest.mark.parametrize("case", ALL_CASES, ids=[c[0] for c in ALL_CASES])
 def test_multi_query_matches_oracle(case):
-    name, B, Hq, Hkv, D, Tq, window, paged, int8, lens = case
+    name, B, Hq, Hkv, D, Tq, window, paged, int8, lens, big_cap = case
     wl = Workload(name, B, Hq, Hkv, D, paged=paged, v_int8=int8, window=window,
                   seed=900 + len(name))
-    cap = max(lens)
+    cap = big_cap or max(lens)
     if not paged:
         cap = -(-cap // 16) * 16
     inp = build_case(wl, seq_lens=lens, capacity=cap, spare_blocks=2 if paged else 0)

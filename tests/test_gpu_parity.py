@@ -307,6 +307,20 @@ def test_many_rows_take_the_warp_per_row_merge(D, int8):
     assert np.all(got[3] == 0)
 
 
+@pytest.mark.parametrize("D,Hq,int8", [(128, 32, False), (128, 32, True), (256, 32, False)])
+def test_sixteen_query_heads_per_kv_head_take_two_column_groups(D, Hq, int8):
+    """G = 16 with a block table of 2^20 tokens per sequence: the K/V the
+    capacity allows passes the two-group threshold, so a warp carries 16
+    columns (at D=256 with the query rows in shared memory)."""
+    wl = W(f"two_groups_{D}_{int(int8)}", 3, Hq, 2, D, paged=True, v_int8=int8, window=500,
+           window_odd_only=True)
+    lens = [20000, 9, 1700]
+    inp = build_case(wl, seq_lens=lens, capacity=1 << 20, spare_blocks=2)
+    want = oracle_decode(wl, inp)
+    got = gpu_decode(wl, to_cuda(inp)).cpu().numpy()
+    assert_close(got, want, int8, wl.name)
+
+
 def test_one_long_unit_spans_every_worker():
     """One sequence, one KV head, one query head: the unit's partials come
     from every worker of the grid, so the merge folds more than 512 slots in
