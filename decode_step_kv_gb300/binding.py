@@ -55,6 +55,15 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
             lib.fa_decode_batch_invariant_workspace_size.argtypes = [i32, i32, i32, i32, i32,
                                                                      i32]
             lib.fa_decode_batch_invariant_workspace_size.restype = sz
+            lib.fa_decode_multi_batch_invariant.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32,
+                                                            f32, P, P, i32, i32, i32, i32, i32, P,
+                                                            sz, P]
+            lib.fa_decode_multi_batch_invariant.restype = i32
+            lib.fa_decode_multi_batch_invariant_workspace_size.argtypes = [i32] * 7
+            lib.fa_decode_multi_batch_invariant_workspace_size.restype = sz
+            lib.fa_decode_ring_batch_invariant.argtypes = [P, P, P, P, P, i32, i32, i32, f32, P,
+                                                           P, i32, i32, i32, P, sz, P]
+            lib.fa_decode_ring_batch_invariant.restype = i32
             lib.fa_decode_multi.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, f32, P, P, i32,
                                             i32, i32, i32, P, sz, P]
             lib.fa_decode_multi.restype = i32
@@ -160,6 +169,43 @@ def fa_decode_batch_invariant_workspace_size(batch, n_q_heads, n_kv_heads, head_
                                              split_tokens=512) -> int:
     return int(load().fa_decode_batch_invariant_workspace_size(
         batch, n_q_heads, n_kv_heads, head_dim, max_kv_len, split_tokens))
+
+
+def fa_decode_multi_batch_invariant(q, k_cache, v_cache, v_scales, block_table, seq_lens,
+                                    n_q_heads, n_kv_heads, head_dim, scale, window, out, *,
+                                    split_tokens=512, page_size=16, max_blocks_per_seq=None,
+                                    num_blocks=None, workspace=None, stream=None):
+    """fa_decode_multi with the batch-invariant plan (fixed splits per sequence)."""
+    batch, tq = q.shape[0], q.shape[1]
+    if max_blocks_per_seq is None:
+        max_blocks_per_seq = block_table.shape[1] if block_table is not None else k_cache.shape[2]
+    if num_blocks is None:
+        num_blocks = k_cache.shape[0] if block_table is not None else 0
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = load().fa_decode_multi_batch_invariant(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(v_scales), _ptr(block_table),
+        _ptr(seq_lens), int(tq), int(n_q_heads), int(n_kv_heads), int(head_dim), float(scale),
+        _ptr(window), _ptr(out), int(batch), int(page_size), int(max_blocks_per_seq),
+        int(num_blocks), int(split_tokens), _ptr(workspace), ws_bytes, _stream(stream))
+    _check(rc)
+
+
+def fa_decode_multi_batch_invariant_workspace_size(batch, n_queries, n_q_heads, n_kv_heads,
+                                                   head_dim, max_kv_len, split_tokens=512) -> int:
+    return int(load().fa_decode_multi_batch_invariant_workspace_size(
+        batch, n_queries, n_q_heads, n_kv_heads, head_dim, max_kv_len, split_tokens))
+
+
+def fa_decode_ring_batch_invariant(q, k_cache, v_cache, v_scales, seq_lens, n_q_heads,
+                                   n_kv_heads, head_dim, scale, window, out, *, split_tokens=512,
+                                   workspace=None, stream=None):
+    """fa_decode_ring with the batch-invariant plan (fixed splits per sequence)."""
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = load().fa_decode_ring_batch_invariant(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(v_scales), _ptr(seq_lens), int(n_q_heads),
+        int(n_kv_heads), int(head_dim), float(scale), _ptr(window), _ptr(out), int(q.shape[0]),
+        int(k_cache.shape[2]), int(split_tokens), _ptr(workspace), ws_bytes, _stream(stream))
+    _check(rc)
 
 
 def fa_decode_multi(q, k_cache, v_cache, v_scales, block_table, seq_lens, n_q_heads, n_kv_heads,

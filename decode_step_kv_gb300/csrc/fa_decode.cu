@@ -2487,6 +2487,62 @@ FA_API size_t fa_decode_batch_invariant_workspace_size(int batch, int n_q_heads,
     return plan_workspace(pl, batch, n_q_heads, head_dim);
 }
 
+FA_API size_t fa_decode_multi_batch_invariant_workspace_size(int batch, int n_queries,
+                                                             int n_q_heads, int n_kv_heads,
+                                                             int head_dim, int max_kv_len,
+                                                             int split_tokens)
+{
+    if (n_queries <= 0 || n_queries > 256 || batch <= 0 || n_q_heads <= 0 || n_kv_heads <= 0 ||
+        n_q_heads % n_kv_heads || (head_dim != 128 && head_dim != 256) || max_kv_len < 0 ||
+        !split_tokens_ok(split_tokens))
+        return 0;
+    const Plan pl = make_plan(Path::Mma, batch, n_q_heads, n_kv_heads, head_dim, max_kv_len, 1,
+                              false, n_queries, split_tokens / 16);
+    return plan_workspace(pl, batch, n_q_heads, head_dim);
+}
+
+FA_API int fa_decode_multi_batch_invariant(const void *q, const void *k_cache,
+                                           const void *v_cache, const void *v_scales,
+                                           const int32_t *block_table, const int32_t *seq_lens,
+                                           int n_queries, int n_q_heads, int n_kv_heads,
+                                           int head_dim, float scale, const int32_t *window,
+                                           void *out, int batch, int page_size,
+                                           int max_blocks_per_seq, int num_blocks,
+                                           int split_tokens, void *workspace,
+                                           size_t workspace_bytes, void *stream)
+{
+    g_err[0] = 0;
+    if (n_queries <= 0 || n_queries > 256)
+        return fail(FA_ERR_LAYOUT, "fa_decode_multi_batch_invariant: n_queries %d must be in "
+                                   "[1, 256]", n_queries);
+    if (!split_tokens_ok(split_tokens))
+        return fail(FA_ERR_LAYOUT, "fa_decode_multi_batch_invariant: split_tokens %d must be a "
+                                   "positive multiple of 16", split_tokens);
+    return decode_impl(q, k_cache, v_cache, v_scales, block_table, seq_lens, n_q_heads,
+                       n_kv_heads, head_dim, scale, window, out, batch, page_size,
+                       max_blocks_per_seq, num_blocks, workspace, workspace_bytes, stream, false,
+                       n_queries, split_tokens / 16);
+}
+
+FA_API int fa_decode_ring_batch_invariant(const void *q, const void *k_cache,
+                                          const void *v_cache, const void *v_scales,
+                                          const int32_t *seq_lens, int n_q_heads, int n_kv_heads,
+                                          int head_dim, float scale, const int32_t *window,
+                                          void *out, int batch, int capacity, int split_tokens,
+                                          void *workspace, size_t workspace_bytes, void *stream)
+{
+    g_err[0] = 0;
+    if (capacity <= 0 || capacity % 16)
+        return fail(FA_ERR_LAYOUT, "fa_decode_ring_batch_invariant: capacity %d must be a "
+                                   "positive multiple of 16", capacity);
+    if (!split_tokens_ok(split_tokens))
+        return fail(FA_ERR_LAYOUT, "fa_decode_ring_batch_invariant: split_tokens %d must be a "
+                                   "positive multiple of 16", split_tokens);
+    return decode_impl(q, k_cache, v_cache, v_scales, nullptr, seq_lens, n_q_heads, n_kv_heads,
+                       head_dim, scale, window, out, batch, 16, capacity, 0, workspace,
+                       workspace_bytes, stream, true, 1, split_tokens / 16);
+}
+
 FA_API int fa_decode_multi(const void *q, const void *k_cache, const void *v_cache,
                            const void *v_scales, const int32_t *block_table,
                            const int32_t *seq_lens, int n_queries, int n_q_heads, int n_kv_heads,

@@ -148,6 +148,38 @@ FA_API size_t fa_decode_batch_invariant_workspace_size(int batch, int n_q_heads,
                                                        int split_tokens);
 
 /*
+ * The batch-invariant plan for the other two decode forms, with the same
+ * guarantee (a sequence's bytes do not depend on the rest of the batch):
+ *   fa_decode_multi_batch_invariant -- fa_decode_multi's arguments plus
+ *     split_tokens; workspace of
+ *     fa_decode_multi_batch_invariant_workspace_size() bytes;
+ *   fa_decode_ring_batch_invariant -- fa_decode_ring's arguments plus
+ *     split_tokens; workspace of fa_decode_batch_invariant_workspace_size(
+ *     batch, n_q_heads, n_kv_heads, head_dim, capacity + 16, split_tokens)
+ *     bytes (a ring's attended range can straddle one more tile).
+ * Rules and errors as the forms they extend and as fa_decode_batch_invariant.
+ */
+FA_API int fa_decode_multi_batch_invariant(const void *q, const void *k_cache,
+                                           const void *v_cache, const void *v_scales,
+                                           const int32_t *block_table, const int32_t *seq_lens,
+                                           int n_queries, int n_q_heads, int n_kv_heads,
+                                           int head_dim, float scale, const int32_t *window,
+                                           void *out, int batch, int page_size,
+                                           int max_blocks_per_seq, int num_blocks,
+                                           int split_tokens, void *workspace,
+                                           size_t workspace_bytes, void *stream);
+FA_API size_t fa_decode_multi_batch_invariant_workspace_size(int batch, int n_queries,
+                                                             int n_q_heads, int n_kv_heads,
+                                                             int head_dim, int max_kv_len,
+                                                             int split_tokens);
+FA_API int fa_decode_ring_batch_invariant(const void *q, const void *k_cache,
+                                          const void *v_cache, const void *v_scales,
+                                          const int32_t *seq_lens, int n_q_heads, int n_kv_heads,
+                                          int head_dim, float scale, const int32_t *window,
+                                          void *out, int batch, int capacity, int split_tokens,
+                                          void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * fa_decode_multi -- several query tokens per sequence in one call: the
  * speculative-verify form of the decode step (the n_queries field of the
  * pages' params; causal rule of tessl's flash_attn_rows on the "nn.rs" page).

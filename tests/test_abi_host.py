@@ -165,3 +165,25 @@ def test_batch_invariant_rejects_bad_split_and_sizes_its_workspace(lib):
     assert g(1, 8, 2, 128, 512, 16) == 32 * one
     assert g(3, 8, 2, 128, 512, 512) == 3 * one
     assert g(1, 8, 2, 128, 513, 512) == 2 * one
+
+
+def test_batch_invariant_multi_and_ring_reject_bad_arguments(lib):
+    f = lib.fa_decode_multi_batch_invariant
+    #               q  k      v      vs    bt    sl     tq hq hkv d    scale win  out    B  P   maxb
+    args = lambda tq, st: (A, 2 * A, 3 * A, None, None, 4 * A, tq, 8, 2, 128, 0.1, None, 5 * A, 1,
+                           16, 512, 0, st, 6 * A, 1 << 30, None)
+    assert f(*args(0, 512)) == -6 and f(*args(257, 512)) == -6
+    assert f(*args(4, 24)) == -6 and f(*args(4, 0)) == -6
+    g = lib.fa_decode_ring_batch_invariant
+    #        q  k      v      vs    sl     hq hkv d    scale win  out    B  cap  st   ws     wsb
+    assert g(A, 2 * A, 3 * A, None, 4 * A, 8, 2, 128, 0.1, None, 5 * A, 1, 100, 512, 6 * A,
+             1 << 30, None) == -6
+    assert g(A, 2 * A, 3 * A, None, 4 * A, 8, 2, 128, 0.1, None, 5 * A, 1, 64, 40, 6 * A,
+             1 << 30, None) == -6
+    h = lib.fa_decode_multi_batch_invariant_workspace_size
+    assert h(1, 0, 8, 2, 128, 512, 512) == 0 and h(1, 4, 8, 2, 128, 512, 24) == 0
+    # one query is the single-query plan; 4 queries x G=4 = 16 columns = two
+    # 8-column units per KV head
+    assert h(1, 1, 8, 2, 128, 512, 512) == lib.fa_decode_batch_invariant_workspace_size(
+        1, 8, 2, 128, 512, 512)
+    assert h(1, 4, 8, 2, 128, 512, 512) == 2 * 2 * 1 * 8 * (128 * 4 + 8)

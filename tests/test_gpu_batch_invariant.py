@@ -12,6 +12,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from decode_step_kv_gb300 import binding
 from decode_step_kv_gb300.inputs import Workload
 
@@ -107,3 +108,85 @@ def test_stream_k_plan_is_batch_dependent_but_close():
                       dinp["seq_lens"], wl.n_q_heads, wl.n_kv_heads, wl.head_dim, wl.scale, None,
                       out, workspace=ws)
     assert_close(out.cpu().numpy(), inv, False, "stream-K vs batch-invariant")
+
+
+def _multi(wl, d, q, tq, st, rows):
+    idx = torch.tensor(rows, device="cuda")
+    qq = q.index_select(0, idx).contiguous()
+    sl = d["seq_lens"].index_select(0, idx).contiguous()
+    bt = d["block_table"].index_select(0, idx).contiguous()
+    win = None if d["window"] is None else d["window"].index_select(0, idx).contiguous()
+    B = len(rows)
+    cap = d["max_blocks"] * wl.page_size
+    n = binding.fa_decode_multi_batch_invariant_workspace_size(B, tq, wl.n_q_heads, wl.n_kv_heads,
+                                                               wl.head_dim, cap, st)
+    ws = torch.full((max(n, 16),), 0xFF, dtype=torch.uint8, device="cuda")
+    out = torch.full((B, tq, wl.n_q_heads, wl.head_dim), float("nan"), device="cuda")
+    binding.fa_decode_multi_batch_invariant(qq, d["k_cache"], d["v_cache"], d.get("v_scales"), bt,
+                                            sl, wl.n_q_heads, wl.n_kv_heads, wl.head_dim,
+                                            wl.scale, win, out, split_tokens=st,
+                                            max_blocks_per_seq=d["max_blocks"],
+                                            num_blocks=d["num_blocks"], workspace=ws)
+    torch.cuda.synchronize()
+    return out.cpu()
+
+
+@pytest.mark.parametrize("D,int8,tq,st", [(128, False, 3, 256), (256, True, 5, 64)])
+def test_multi_query_batch_invariant(D, int8, tq, st):
+    """Several queries per sequence (columns beyond 8 span two units): the
+    oracle's multi-query mode, and bit-identical rows alone and reordered."""
+    wl = W(f"bi_multi_{D}_{int(int8)}", 5, 8, 2, D, paged=True, v_int8=int8, window=400,
+           window_odd_only=True)
+    lens = [1, 700, 2100, 33, 1300]
+    inp = build_case(wl, seq_lens=lens, spare_blocks=2)
+    q = np.random.default_rng(D + tq).standard_normal((5, tq, 8, D)).astype(np.float16)
+    d = to_cuda(inp)
+    qd = torch.from_numpy(q).cuda()
+    whole = _multi(wl, d, qd, tq, st, list(range(5)))
+    want = oracle.decode_multi(q, inp["k_cache"].numpy(), inp["v_cache"].numpy(), lens,
+                               scale=wl.scale, n_kv_heads=2,
+                               v_scales=None if not int8 else inp["v_scales"].numpy(),
+                               block_table=inp["block_table"].numpy(),
+                               window=inp["window"].numpy(), page_size=16,
+                               max_blocks=inp["max_blocks"])
+    assert_close(whole.numpy(), want, int8, wl.name)
+    for b in range(5):
+        assert torch.equal(_multi(wl, d, qd, tq, st, [b])[0], whole[b]), f"sequence {b} alone"
+    perm = [3, 0, 4, 2, 1]
+    got = _multi(wl, d, qd, tq, st, perm)
+    for i, b in enumerate(perm):
+        assert torch.equal(got[i], whole[b]), f"sequence {b} reordered"
+
+
+def test_ring_batch_invariant():
+    C = 128
+    B, Hq, Hkv, D = 4, 8, 2, 128
+    seen = [5, 128, 300, 1000]
+    g = np.random.default_rng(77)
+    q = g.standard_normal((B, Hq, D)).astype(np.float16)
+    k = g.standard_normal((B, Hkv, C, D)).astype(np.float16)
+    v = g.standard_normal((B, Hkv, C, D)).astype(np.float16)
+    win = np.array([0, 50, 0, 100], dtype=np.int32)
+    scale = D ** -0.5
+    want = oracle.decode_ring(q, k, v, seen, scale=scale, n_kv_heads=Hkv, window=win)
+    qd, kd, vd = (torch.from_numpy(x).cuda() for x in (q, k, v))
+    sl = torch.tensor(seen, dtype=torch.int32, device="cuda")
+    wd = torch.from_numpy(win).cuda()
+
+    def run(rows, st=32):
+        idx = torch.tensor(rows, device="cuda")
+        n = binding.fa_decode_batch_invariant_workspace_size(len(rows), Hq, Hkv, D, C + 16, st)
+        ws = torch.full((max(n, 16),), 0xFF, dtype=torch.uint8, device="cuda")
+        out = torch.full((len(rows), Hq, D), float("nan"), device="cuda")
+        binding.fa_decode_ring_batch_invariant(
+            qd.index_select(0, idx).contiguous(), kd.index_select(0, idx).contiguous(),
+            vd.index_select(0, idx).contiguous(), None, sl.index_select(0, idx).contiguous(),
+            Hq, Hkv, D, scale, wd.index_select(0, idx).contiguous(), out, split_tokens=st,
+            workspace=ws)
+        torch.cuda.synchronize()
+        return out.cpu()
+
+    whole = run(list(range(B)))
+    assert_close(whole.numpy(), want, False, "ring batch-invariant")
+    for b in range(B):
+        assert torch.equal(run([b])[0], whole[b]), f"ring sequence {b} alone"
