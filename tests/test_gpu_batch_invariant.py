@@ -190,3 +190,24 @@ def test_ring_batch_invariant():
     assert_close(whole.numpy(), want, False, "ring batch-invariant")
     for b in range(B):
         assert torch.equal(run([b])[0], whole[b]), f"ring sequence {b} alone"
+
+
+def test_batch_invariant_flags_clamped_lengths_and_bad_blocks():
+    """The batch-invariant plan reads lengths and block ids through the same
+    checks: a length beyond capacity is clamped and flagged, a block id out
+    of range skips its tile and is flagged, other sequences are unaffected."""
+    wl = W("bi_status", 3, 8, 2, 128, paged=True)
+    inp = build_case(wl, seq_lens=[64, 32, 500])
+    want = oracle_decode(wl, inp)
+    dinp = to_cuda(inp)
+    binding.fa_decode_device_status()                       # clear
+    dinp["seq_lens"] = torch.tensor([64, 10 ** 6, 500], dtype=torch.int32, device="cuda")
+    bt = dinp["block_table"].clone()
+    bt[0, 1] = 10 ** 6                                      # sequence 0 loses its second page
+    dinp["block_table"] = bt
+    got = _run(wl, dinp, 64).numpy()
+    status = binding.fa_decode_device_status()
+    assert status & binding.FA_STATUS_LEN_CLAMPED
+    assert status & binding.FA_STATUS_BAD_BLOCK
+    assert np.all(np.isfinite(got))
+    assert_close(got[2], want[2], False, "untouched sequence 2")
