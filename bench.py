@@ -4,7 +4,7 @@
 One step = one fa_decode call (split-K kernel + log-sum-exp merge kernel)
 over every sequence of the workload, inputs resident in HBM.  The headline
 line is measured on the 4-sequence, 16/8-head, head_dim 256, ragged
-1K-8K workload (cfg2); every other decode workload is measured too and
+1K-8K workload (4x1k-8k_d256); every other decode workload is measured too and
 listed under "configs".
 
 Timing: W untimed warm-up steps, then K timed steps bracketed by a barrier and
@@ -38,7 +38,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "decode attention µs/step and KV-read GB/s (fraction of GB300 HBM peak)"
-HEADLINE = "cfg2"
+HEADLINE = "4x1k-8k_d256"
 L2_BYTES = 129 * 2 ** 20
 FALLBACK_HBM_GBS = 6800.0
 
@@ -375,10 +375,10 @@ def time_next_rows(steps, device, peak):
     stream = torch.cuda.current_stream(device)
     res = {}
 
-    # ring cache: cfg5's heads and lengths (tokens seen ~U[128, 64K]) on a
+    # ring cache: 64x128-64k_d128_win's heads and lengths (tokens seen ~U[128, 64K]) on a
     # 4096-row ring per sequence, the storage of a sliding-window layer
     C = 4096
-    wl = dataclasses.replace(WORKLOADS["cfg5"], name="ring", paged=False, window=0,
+    wl = dataclasses.replace(WORKLOADS["64x128-64k_d128_win"], name="ring", paged=False, window=0,
                              window_odd_only=False)
     d = make_inputs(wl, device, capacity=C)
     B, Hq, Hkv, D = wl.batch, wl.n_q_heads, wl.n_kv_heads, wl.head_dim
@@ -396,10 +396,10 @@ def time_next_rows(steps, device, peak):
     del d, ws, out
     torch.cuda.empty_cache()
 
-    # multi-query decode (speculative verify) on cfg3's shape: with G = 4,
+    # multi-query decode (speculative verify) on 32x32k_d128_paged's shape: with G = 4,
     # 2 queries make 8 (query, head) columns per KV head (one column group),
     # 4 queries make 16 (two groups, so each K/V tile is read twice)
-    wl = WORKLOADS["cfg3"]
+    wl = WORKLOADS["32x32k_d128_paged"]
     d = prepare(wl, device)
     B, Hq, Hkv, D = wl.batch, wl.n_q_heads, wl.n_kv_heads, wl.head_dim
     nbytes = kv_bytes(wl, d["lens"], None)
@@ -415,15 +415,15 @@ def time_next_rows(steps, device, peak):
             workspace=ws, stream=stream), nbytes, steps, 3, device)
         gbs = nbytes / (us * 1e-6) / 1e9
         res[f"multi_query_tq{tq}"] = {
-            "workload": f"cfg3 shape (32 x 32K, 32 q/8 kv heads, D=128, paged), {tq} queries "
+            "workload": f"32x32k_d128_paged shape (32 x 32K, 32 q/8 kv heads, D=128, paged), {tq} queries "
                         "per sequence", "us_per_step": round(us, 2), "kv_bytes": nbytes,
             "GB/s": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4),
             "column_groups": -(-tq * wl.group // 8)}
         del ws, out, q
 
-    # multi-query decode at D=256: cfg4's shape with fp16 V and 8 queries (16
+    # multi-query decode at D=256: 16x16k_d256_int8v's shape with fp16 V and 8 queries (16
     # columns per KV head: two groups per warp, the query rows in shared memory)
-    wl2 = dataclasses.replace(WORKLOADS["cfg4"], name="cfg4_fp16", v_int8=False)
+    wl2 = dataclasses.replace(WORKLOADS["16x16k_d256_int8v"], name="16x16k_d256_fp16v", v_int8=False)
     d2 = prepare(wl2, device)
     B2, Hq2, Hkv2, D2 = wl2.batch, wl2.n_q_heads, wl2.n_kv_heads, wl2.head_dim
     nbytes2 = kv_bytes(wl2, d2["lens"], None)
@@ -438,17 +438,17 @@ def time_next_rows(steps, device, peak):
         workspace=ws, stream=stream), nbytes2, steps, 3, device)
     gbs = nbytes2 / (us * 1e-6) / 1e9
     res["multi_query_d256_tq8"] = {
-        "workload": "16 x 16K, 16 q/8 kv heads, D=256, paged, fp16 V (cfg4 with fp16 V), "
+        "workload": "16 x 16K, 16 q/8 kv heads, D=256, paged, fp16 V (16x16k_d256_int8v with fp16 V), "
                     "8 queries per sequence", "us_per_step": round(us, 2), "kv_bytes": nbytes2,
         "GB/s": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4), "column_groups": 2}
     del d2, q, ws, out
     torch.cuda.empty_cache()
 
     # cache append: one new K/V row per (sequence, KV head) at each sequence's
-    # last position, into cfg3's paged cache (fp16 V) and cfg4's (int8 V)
+    # last position, into 32x32k_d128_paged's paged cache (fp16 V) and 16x16k_d256_int8v's (int8 V)
     g = torch.Generator(device=device)
     g.manual_seed(wl.seed + 2000)
-    for name, w2 in (("append", wl), ("append_int8", WORKLOADS["cfg4"])):
+    for name, w2 in (("append", wl), ("append_int8", WORKLOADS["16x16k_d256_int8v"])):
         dd = d if w2 is wl else prepare(w2, device)
         B, Hkv, D = w2.batch, w2.n_kv_heads, w2.head_dim
         k_new = torch.randn((B, Hkv, D), generator=g, device=device)
@@ -717,7 +717,7 @@ def run_ours(args, world, rank, local):
         line["next_rows"] = time_next_rows(max(10, min(args.steps, 30)), device, peak)
         line["batch_invariant"] = {
             "split_tokens": list(BI_SPLIT_TOKENS),
-            "note": "configs[*].batch_invariant_us_per_step[split_tokens]: "
+            "note": "each workload entry's batch_invariant_us_per_step[split_tokens]: "
                     "fa_decode_batch_invariant on the same inputs and protocol (fixed splits "
                     "per sequence, bit-identical whatever the batch)"}
     if rank == 0 and world == 1 and not args.no_cpu:

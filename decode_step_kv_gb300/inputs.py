@@ -16,11 +16,11 @@ Recipe (the same for every workload):
   * ragged lengths: either listed or drawn uniform in [lo, hi] by randint.
 
 The five named workloads are the decode shapes the method is measured on:
-  cfg1  1 seq, 8 q / 2 kv heads, D 128, L 512, contiguous fp16
-  cfg2  4 seqs, 16 q / 8 kv heads, D 256, L {1024, 2048, 4096, 8192}, contiguous
-  cfg3  32 seqs, 32 q / 8 kv heads, D 128, L 32768, paged (split-K long context)
-  cfg4  16 seqs, 16 q / 8 kv heads, D 256, L 16384, paged, K fp16 + V int8
-  cfg5  64 seqs, 32 q / 4 kv heads, D 128, L ~ U[128, 65536], paged,
+  1x512_d128  1 seq, 8 q / 2 kv heads, D 128, L 512, contiguous fp16
+  4x1k-8k_d256  4 seqs, 16 q / 8 kv heads, D 256, L {1024, 2048, 4096, 8192}, contiguous
+  32x32k_d128_paged  32 seqs, 32 q / 8 kv heads, D 128, L 32768, paged (split-K long context)
+  16x16k_d256_int8v  16 seqs, 16 q / 8 kv heads, D 256, L 16384, paged, K fp16 + V int8
+  64x128-64k_d128_win  64 seqs, 32 q / 4 kv heads, D 128, L ~ U[128, 65536], paged,
         sliding window 4096 on odd-indexed sequences
 """
 from __future__ import annotations
@@ -60,23 +60,23 @@ class Workload:
 
 
 WORKLOADS = {
-    "cfg1": Workload("cfg1", 1, 8, 2, 128, seq_lens=(512,), seed=BASE_SEED + 0),
-    "cfg2": Workload("cfg2", 4, 16, 8, 256, seq_lens=(1024, 2048, 4096, 8192),
+    "1x512_d128": Workload("1x512_d128", 1, 8, 2, 128, seq_lens=(512,), seed=BASE_SEED + 0),
+    "4x1k-8k_d256": Workload("4x1k-8k_d256", 4, 16, 8, 256, seq_lens=(1024, 2048, 4096, 8192),
                      seed=BASE_SEED + 1),
-    "cfg3": Workload("cfg3", 32, 32, 8, 128, seq_lens=(32768,) * 32, paged=True,
+    "32x32k_d128_paged": Workload("32x32k_d128_paged", 32, 32, 8, 128, seq_lens=(32768,) * 32, paged=True,
                      seed=BASE_SEED + 2),
-    "cfg4": Workload("cfg4", 16, 16, 8, 256, seq_lens=(16384,) * 16, paged=True,
+    "16x16k_d256_int8v": Workload("16x16k_d256_int8v", 16, 16, 8, 256, seq_lens=(16384,) * 16, paged=True,
                      v_int8=True, seed=BASE_SEED + 3),
-    "cfg5": Workload("cfg5", 64, 32, 4, 128, len_range=(128, 65536), paged=True,
+    "64x128-64k_d128_win": Workload("64x128-64k_d128_win", 64, 32, 4, 128, len_range=(128, 65536), paged=True,
                      window=4096, window_odd_only=True, seed=BASE_SEED + 4),
 }
 
 WORKLOAD_DESCRIPTIONS = {
-    "cfg1": "1 seq, 8 q/2 kv heads, D=128, L=512, contiguous fp16 K/V",
-    "cfg2": "4 seqs, 16 q/8 kv heads, D=256, L={1024,2048,4096,8192}, contiguous fp16 K/V",
-    "cfg3": "32 seqs, 32 q/8 kv heads, D=128, L=32768, paged 16-token pages, fp16 K/V",
-    "cfg4": "16 seqs, 16 q/8 kv heads, D=256, L=16384, paged, fp16 K + int8 V (fp16 scale/32)",
-    "cfg5": "64 seqs, 32 q/4 kv heads, D=128, L~U[128,65536], paged, window 4096 on odd seqs",
+    "1x512_d128": "1 seq, 8 q/2 kv heads, D=128, L=512, contiguous fp16 K/V",
+    "4x1k-8k_d256": "4 seqs, 16 q/8 kv heads, D=256, L={1024,2048,4096,8192}, contiguous fp16 K/V",
+    "32x32k_d128_paged": "32 seqs, 32 q/8 kv heads, D=128, L=32768, paged 16-token pages, fp16 K/V",
+    "16x16k_d256_int8v": "16 seqs, 16 q/8 kv heads, D=256, L=16384, paged, fp16 K + int8 V (fp16 scale/32)",
+    "64x128-64k_d128_win": "64 seqs, 32 q/4 kv heads, D=128, L~U[128,65536], paged, window 4096 on odd seqs",
 }
 
 

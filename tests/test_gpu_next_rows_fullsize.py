@@ -1,7 +1,7 @@
 """Parity at the sizes the benchmark times for the rows beyond the plain
 decode step: multi-query decode (4 queries) and the batch-invariant plan on
 the 32 x 32K, 32/8-head, D=128 paged workload, and ring decode on 64
-sequences with cfg5's heads and lengths over 4096-row rings.  The oracle
+sequences with 64x128-64k_d128_win's heads and lengths over 4096-row rings.  The oracle
 recomputes a sample of the sequences (every output row of each), each from a
 host copy of that sequence's cache alone.
 """
@@ -36,8 +36,8 @@ def _seq_blocks(d, b, P):
 
 
 @pytest.fixture(scope="module")
-def cfg3():
-    wl = WORKLOADS["cfg3"]
+def long_context():
+    wl = WORKLOADS["32x32k_d128_paged"]
     torch.cuda.empty_cache()
     d = make_inputs(wl, "cuda")
     yield wl, d
@@ -45,9 +45,9 @@ def cfg3():
     torch.cuda.empty_cache()
 
 
-def test_multi_query_four_queries_at_full_size(cfg3):
+def test_multi_query_four_queries_at_full_size(long_context):
     """16 (query, head) columns per KV head: the two-column-group kernel."""
-    wl, d = cfg3
+    wl, d = long_context
     tq = 4
     B, Hq, Hkv, D = wl.batch, wl.n_q_heads, wl.n_kv_heads, wl.head_dim
     q = make_queries(wl, tq, "cuda")
@@ -69,8 +69,8 @@ def test_multi_query_four_queries_at_full_size(cfg3):
         assert_close(got[b:b + 1], want, False, f"multi-query sequence {b}")
 
 
-def test_batch_invariant_1024_at_full_size(cfg3):
-    wl, d = cfg3
+def test_batch_invariant_1024_at_full_size(long_context):
+    wl, d = long_context
     B, Hq, Hkv, D = wl.batch, wl.n_q_heads, wl.n_kv_heads, wl.head_dim
     cap = d["max_blocks"] * wl.page_size
     n = binding.fa_decode_batch_invariant_workspace_size(B, Hq, Hkv, D, cap, 1024)
@@ -91,7 +91,7 @@ def test_batch_invariant_1024_at_full_size(cfg3):
 
 def test_ring_decode_at_bench_size():
     C = 4096
-    wl = dataclasses.replace(WORKLOADS["cfg5"], name="ring", paged=False, window=0,
+    wl = dataclasses.replace(WORKLOADS["64x128-64k_d128_win"], name="ring", paged=False, window=0,
                              window_odd_only=False)
     torch.cuda.empty_cache()
     d = make_inputs(wl, "cuda", capacity=C)

@@ -230,7 +230,7 @@ def _oracle_rows_paged(wl, dinp, rows, v_codes=None, v_scales=None):
     return res
 
 
-@pytest.mark.parametrize("name", ["cfg1", "cfg2"])
+@pytest.mark.parametrize("name", ["1x512_d128", "4x1k-8k_d256"])
 def test_small_workloads_full_oracle(name, kernel):
     wl = WORKLOADS[name]
     inp = build_case(wl)
@@ -239,7 +239,7 @@ def test_small_workloads_full_oracle(name, kernel):
     assert_close(got, want, wl.v_int8, name)
 
 
-@pytest.mark.parametrize("name", ["cfg3", "cfg4", "cfg5"])
+@pytest.mark.parametrize("name", ["32x32k_d128_paged", "16x16k_d256_int8v", "64x128-64k_d128_win"])
 def test_full_size_workloads_sampled(name):
     wl = WORKLOADS[name]
     torch.cuda.empty_cache()
