@@ -23,6 +23,7 @@ def _tree(tmp_path, source_text):
 def test_traffic_is_read_only_for_the_source_it_was_taken_on(tmp_path, monkeypatch):
     real = open(os.path.join(ROOT, SRC), "rb").read()
     committed = bench.recorded_traffic("fa_stream_mma_kernel", "4x1k-8k_d256")
+    assert committed is not None and committed > 0      # the committed summary matches the tree
     _tree(tmp_path, real)
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     assert bench.recorded_traffic("fa_stream_mma_kernel", "4x1k-8k_d256") == committed
