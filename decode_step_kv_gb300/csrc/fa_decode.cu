@@ -2111,8 +2111,9 @@ static int next_pow2(int x)
 
 // Which split kernel serves a call: the tensor-core kernel, unless
 // FA_DECODE_KERNEL=simt selects the CUDA-core one (for A/B measurements; both
-// compute the same result within the tolerances) or the cache is too large
-// for 32-bit TMA row coordinates.
+// compute the same result within the tolerances).  decode_impl also takes the
+// CUDA-core kernel for caches of 2^31 rows or more, beyond 32-bit TMA row
+// coordinates.
 static Path choose_path()
 {
     const char *e = getenv("FA_DECODE_KERNEL");
@@ -2204,12 +2205,21 @@ static Plan make_plan(Path path, int B, int Hq, int Hkv, int D, long long cap, i
     return pl;
 }
 
+// plan_workspace's answer when the bytes do not fit in a size_t
+constexpr size_t WS_OVERFLOW = ~(size_t)0;
+
 static size_t plan_workspace(const Plan &pl, int B, int Hq, int D)
 {
     if (pl.path == Path::Mma && pl.chunk > 0) {
-        // batch-invariant plan: one partial slot per (unit, chunk)
-        const size_t slots = (size_t)B * pl.units * pl.max_chunks;
-        return slots * pl.sh * (D * sizeof(float) + sizeof(float2));
+        // batch-invariant plan: one partial slot per (unit, chunk); with a
+        // large capacity, short splits and many heads the product can pass
+        // 2^64, and a wrapped size would let a small buffer through
+        size_t n = (size_t)B;
+        for (size_t f : {(size_t)pl.units, (size_t)pl.max_chunks, (size_t)pl.sh,
+                         D * sizeof(float) + sizeof(float2)})
+            if (__builtin_mul_overflow(n, f, &n))
+                return WS_OVERFLOW;
+        return n;
     }
     if (pl.path == Path::Mma) {
         // partial slots: one per (worker, unit) pair, at most W + units
@@ -2369,6 +2379,12 @@ static bool aligned16(const void *x)
     return ((uintptr_t)x & 15u) == 0;
 }
 
+// natural alignment of an element of `bytes` bytes (a null pointer passes)
+static bool aligned_to(const void *x, unsigned bytes)
+{
+    return ((uintptr_t)x & (bytes - 1u)) == 0;
+}
+
 // Scratch for fa_decode_noalloc: a fixed array in the module image, so that
 // entry point needs no allocation.  Host code must not use the symbol's
 // host-side name as a device address; noalloc_scratch() returns the real one.
@@ -2484,7 +2500,8 @@ FA_API size_t fa_decode_batch_invariant_workspace_size(int batch, int n_q_heads,
         return 0;
     const Plan pl = make_plan(Path::Mma, batch, n_q_heads, n_kv_heads, head_dim, max_kv_len, 1,
                               false, 1, split_tokens / 16);
-    return plan_workspace(pl, batch, n_q_heads, head_dim);
+    const size_t n = plan_workspace(pl, batch, n_q_heads, head_dim);
+    return n == WS_OVERFLOW ? 0 : n;
 }
 
 FA_API size_t fa_decode_multi_batch_invariant_workspace_size(int batch, int n_queries,
@@ -2498,7 +2515,8 @@ FA_API size_t fa_decode_multi_batch_invariant_workspace_size(int batch, int n_qu
         return 0;
     const Plan pl = make_plan(Path::Mma, batch, n_q_heads, n_kv_heads, head_dim, max_kv_len, 1,
                               false, n_queries, split_tokens / 16);
-    return plan_workspace(pl, batch, n_q_heads, head_dim);
+    const size_t n = plan_workspace(pl, batch, n_q_heads, head_dim);
+    return n == WS_OVERFLOW ? 0 : n;
 }
 
 FA_API int fa_decode_multi_batch_invariant(const void *q, const void *k_cache,
@@ -2640,6 +2658,9 @@ static int decode_impl(const void *q, const void *k_cache, const void *v_cache,
         (vi8 && !aligned16(v_scales)) || (workspace && !aligned16(workspace)))
         return fail(FA_ERR_ALIGN, "fa_decode: q, k_cache, v_cache, v_scales, out and workspace "
                                   "must be 16-byte aligned");
+    if (!aligned_to(seq_lens, 4) || !aligned_to(block_table, 4) || !aligned_to(window, 4))
+        return fail(FA_ERR_ALIGN, "fa_decode: seq_lens, block_table and window must be 4-byte "
+                                  "aligned");
     const int D = head_dim;
     // aliasing: out against every input range we can size
     const size_t out_bytes = (size_t)batch * tq * n_q_heads * D * sizeof(float);
@@ -2676,6 +2697,8 @@ static int decode_impl(const void *q, const void *k_cache, const void *v_cache,
     const Plan pl = make_plan(path, batch, n_q_heads, n_kv_heads, D, ring ? cap + 16 : cap, sms,
                               vi8, tq, chunk);
     const size_t need = plan_workspace(pl, batch, n_q_heads, D);
+    if (need == WS_OVERFLOW)
+        return fail(FA_ERR_WORKSPACE, "fa_decode: the workspace for these sizes exceeds 2^64 bytes");
     if (need > 0 && (!workspace || workspace_bytes < need))
         return fail(FA_ERR_WORKSPACE, "fa_decode: workspace %zu bytes, need %zu", workspace_bytes,
                     need);
@@ -2835,6 +2858,8 @@ FA_API int fa_quantize_v_int8(const float *x, long long n_rows, int head_dim, in
     if (head_dim <= 0 || head_dim % 32 || n_rows < 0)
         return fail(FA_ERR_HEAD_DIM, "fa_quantize_v_int8: head_dim %d must be a positive "
                                      "multiple of 32", head_dim);
+    if (!aligned_to(x, 4) || !aligned_to(scales, 2))
+        return fail(FA_ERR_ALIGN, "fa_quantize_v_int8: x must be 4-byte and scales 2-byte aligned");
     const long long n_blocks = n_rows * (head_dim / 32);
     if (n_blocks == 0)
         return 0;
@@ -2879,6 +2904,10 @@ FA_API int fa_append_kv(const float *k_new, const float *v_new, void *k_cache, v
             overlaps(v_cache, kv_rows * head_dim * (v_scales ? 1 : 2), ins[i], in_bytes[i]) ||
             (v_scales && overlaps(v_scales, kv_rows * (head_dim / 32) * 2, ins[i], in_bytes[i])))
             return fail(FA_ERR_ALIAS, "fa_append_kv: a cache overlaps k_new, v_new or positions");
+    if (!aligned_to(k_new, 4) || !aligned_to(v_new, 4) || !aligned_to(positions, 4) ||
+        !aligned_to(block_table, 4) || !aligned_to(k_cache, 2) ||
+        !aligned_to(v_cache, v_scales ? 1 : 2) || !aligned_to(v_scales, 2))
+        return fail(FA_ERR_ALIGN, "fa_append_kv: a pointer is not aligned to its element type");
     if ((long long)batch * n_kv_heads > 0x7fffffffll)
         return fail(FA_ERR_LAYOUT, "fa_append_kv: too many rows");
     if (batch == 0)
@@ -2925,6 +2954,10 @@ FA_API int fa_append_kv_ring(const float *k_new, const float *v_new, void *k_cac
             overlaps(v_cache, kv_rows * head_dim * (v_scales ? 1 : 2), ins[i], in_bytes[i]) ||
             (v_scales && overlaps(v_scales, kv_rows * (head_dim / 32) * 2, ins[i], in_bytes[i])))
             return fail(FA_ERR_ALIAS, "fa_append_kv_ring: a cache overlaps k_new, v_new or positions");
+    if (!aligned_to(k_new, 4) || !aligned_to(v_new, 4) || !aligned_to(positions, 4) ||
+        !aligned_to(k_cache, 2) || !aligned_to(v_cache, v_scales ? 1 : 2) ||
+        !aligned_to(v_scales, 2))
+        return fail(FA_ERR_ALIGN, "fa_append_kv_ring: a pointer is not aligned to its element type");
     if ((long long)batch * n_kv_heads > 0x7fffffffll)
         return fail(FA_ERR_LAYOUT, "fa_append_kv_ring: too many rows");
     if (batch == 0)
@@ -2962,6 +2995,8 @@ FA_API int fa_gather_kv_debug(const void *cache, int row_bytes, const int32_t *b
     if (n_tokens > cap)
         return fail(FA_ERR_LAYOUT, "fa_gather_kv_debug: n_tokens %d > capacity %lld", n_tokens,
                     cap);
+    if (!aligned_to(block_table, 4))
+        return fail(FA_ERR_ALIGN, "fa_gather_kv_debug: block_table must be 4-byte aligned");
     if (n_tokens == 0)
         return 0;
     Params p = {};

@@ -53,7 +53,7 @@ extern "C" {
 #define FA_ERR_LAYOUT (-6)      /* bad batch / page_size / block counts / capacity */
 #define FA_ERR_ALIAS (-7)       /* out overlaps an input or the workspace */
 #define FA_ERR_CUDA (-8)        /* a CUDA call or kernel launch failed */
-#define FA_ERR_ALIGN (-9)       /* a tensor is not 16-byte aligned */
+#define FA_ERR_ALIGN (-9)       /* a pointer is not aligned as its entry point requires */
 
 /* Device-side status bits, reported by fa_decode_device_status(). */
 #define FA_STATUS_LEN_CLAMPED 1u   /* a seq_lens entry was < 0 or > capacity and was clamped */
@@ -100,7 +100,8 @@ extern "C" {
  *            may be captured in a CUDA graph and replayed with new
  *            device-side lengths.
  *
- * q, k_cache, v_cache, v_scales and out must be 16-byte aligned.
+ * q, k_cache, v_cache, v_scales and out must be 16-byte aligned, and
+ * seq_lens, block_table and window 4-byte aligned (else FA_ERR_ALIGN).
  */
 FA_API int fa_decode(const void *q, const void *k_cache, const void *v_cache,
                      const void *v_scales, const int32_t *block_table,
@@ -142,7 +143,9 @@ FA_API int fa_decode_batch_invariant(const void *q, const void *k_cache, const v
 
 /* Scratch bytes for fa_decode_batch_invariant: one partial (D floats of O
  * plus max and sum) per query head and split of every sequence at
- * max_kv_len keys.  Host-only; 0 for invalid sizes. */
+ * max_kv_len keys.  Host-only; 0 for invalid sizes, and for sizes whose
+ * scratch would not fit in a size_t (the decode call then fails with
+ * FA_ERR_WORKSPACE whatever buffer it is given). */
 FA_API size_t fa_decode_batch_invariant_workspace_size(int batch, int n_q_heads, int n_kv_heads,
                                                        int head_dim, int max_kv_len,
                                                        int split_tokens);
@@ -247,7 +250,8 @@ FA_API size_t fa_decode_workspace_size(int batch, int n_q_heads, int n_kv_heads,
  * s = fp16 round-to-nearest-even(max|x| / 127); code = clamp(round-half-even(
  * x / s), -127, 127), all zero when s == 0.  (The pages print only the
  * dequantisation, ggml block_q8_0 on the DS4Server page "dsv4_hc.metal";
- * this quantiser is the plain symmetric reading.)  head_dim % 32 == 0.
+ * this quantiser is the plain symmetric reading.)  head_dim % 32 == 0; x is
+ * 4-byte and scales 2-byte aligned (else FA_ERR_ALIGN).
  */
 FA_API int fa_quantize_v_int8(const float *x, long long n_rows, int head_dim, int8_t *codes,
                               void *scales, void *stream);
@@ -269,7 +273,8 @@ FA_API int fa_quantize_v_int8(const float *x, long long n_rows, int head_dim, in
  * sequence's rows untouched and sets FA_STATUS_POS_RANGE; an unmapped block
  * id (outside [0, num_blocks)) skips that store and sets FA_STATUS_BAD_BLOCK.
  * head_dim must be a positive multiple of 32.  The caches must not overlap
- * k_new, v_new or positions.
+ * k_new, v_new or positions.  Every pointer is aligned to its element type
+ * (4 bytes for fp32 and int32, 2 for fp16), else FA_ERR_ALIGN.
  */
 FA_API int fa_append_kv(const float *k_new, const float *v_new, void *k_cache, void *v_cache,
                         void *v_scales, const int32_t *block_table, const int32_t *positions,
@@ -293,7 +298,7 @@ FA_API int fa_append_kv_ring(const float *k_new, const float *v_new, void *k_cac
  * exists so the block-table indirection can be checked bit for bit.
  * Block ids are range-checked against num_blocks (FA_ERR_LAYOUT on the host
  * is impossible for device tables; bad ids leave zero rows and set
- * FA_STATUS_BAD_BLOCK).
+ * FA_STATUS_BAD_BLOCK).  block_table is 4-byte aligned (else FA_ERR_ALIGN).
  */
 FA_API int fa_gather_kv_debug(const void *cache, int row_bytes, const int32_t *block_table,
                               int b, int n_kv_heads, int page_size, int max_blocks_per_seq,

@@ -74,6 +74,8 @@ def call(lib, **kw):
     (dict(bt=7 * A, page=16, nblk=0), -6),
     (dict(vs=8 * A, maxb=500), -6),                      # contiguous int8 needs cap % 16 == 0
     (dict(q=A + 8), -9), (dict(out=5 * A + 4), -9), (dict(k=2 * A + 2), -9),
+    (dict(sl=4 * A + 2), -9), (dict(win=8 * A + 1), -9),            # int32 arrays: 4-byte
+    (dict(bt=7 * A + 2, page=16, nblk=10), -9),
     (dict(out=2 * A + 64), -7),                          # out inside the K cache
     (dict(out=A), -7),                                   # out == q
 ])
@@ -105,6 +107,9 @@ def test_quantize_and_gather_reject_bad_arguments(lib):
     assert lib.fa_gather_kv_debug(A, 256, None, 0, 2, 16, 64, 0, 65, A, None) == -6
     assert lib.fa_gather_kv_debug(A, 256, A, 0, 2, 8, 64, 4, 16, A, None) == -6
     assert lib.fa_gather_kv_debug(None, 256, None, 0, 2, 16, 64, 0, 16, A, None) == -1
+    assert lib.fa_gather_kv_debug(A, 256, 5 * A + 2, 0, 2, 16, 64, 4, 16, 6 * A, None) == -9
+    assert lib.fa_quantize_v_int8(A + 2, 1, 32, 2 * A, 3 * A, None) == -9
+    assert lib.fa_quantize_v_int8(A, 1, 32, 2 * A, 3 * A + 1, None) == -9
 
 
 def test_append_rejects_bad_arguments(lib):
@@ -119,6 +124,16 @@ def test_append_rejects_bad_arguments(lib):
     # the K cache (1 x 2 x 64 x 128 fp16 = 32 KiB from 2A) would overlap k_new at 2A + 4096
     assert f(2 * A + 4096, A, 2 * A, 3 * A, None, None, 4 * A, 1, 2, 128, 16, 64, 0, None) == -7
     assert f(A, A, 2 * A, 3 * A, None, None, 4 * A, 0, 2, 128, 16, 64, 0, None) == 0   # no-op
+    # pointers aligned to their element type: fp32 and int32 4 bytes, fp16 2
+    assert f(A + 2, A, 2 * A, 3 * A, None, None, 4 * A, 1, 2, 128, 16, 64, 0, None) == -9
+    assert f(A, A, 2 * A + 1, 3 * A, None, None, 4 * A, 1, 2, 128, 16, 64, 0, None) == -9
+    assert f(A, A, 2 * A, 3 * A + 1, None, None, 4 * A, 1, 2, 128, 16, 64, 0, None) == -9
+    assert f(A, A, 2 * A, 3 * A, 8 * A + 1, None, 4 * A, 1, 2, 128, 16, 64, 0, None) == -9
+    assert f(A, A, 2 * A, 3 * A, None, None, 4 * A + 2, 1, 2, 128, 16, 64, 0, None) == -9
+    assert f(A, A, 2 * A, 3 * A, None, 5 * A + 2, 4 * A, 1, 2, 128, 16, 64, 4, None) == -9
+    g = lib.fa_append_kv_ring
+    #        k_new  v_new  k_cache  v_cache scales pos    B  Hkv D    cap stream
+    assert g(A, A + 1, 2 * A, 3 * A, None, 4 * A, 1, 2, 128, 64, None) == -9
 
 
 def test_ring_rejects_bad_capacity(lib):
@@ -165,6 +180,19 @@ def test_batch_invariant_rejects_bad_split_and_sizes_its_workspace(lib):
     assert g(1, 8, 2, 128, 512, 16) == 32 * one
     assert g(3, 8, 2, 128, 512, 512) == 3 * one
     assert g(1, 8, 2, 128, 513, 512) == 2 * one
+
+
+def test_batch_invariant_workspace_size_does_not_wrap(lib):
+    """The scratch grows with batch x units x splits; where that passes 2^64
+    bytes the size is 0 (invalid) rather than the wrapped remainder."""
+    g = lib.fa_decode_batch_invariant_workspace_size
+    h = lib.fa_decode_multi_batch_invariant_workspace_size
+    B, Hkv, G, D, L = 65535, 4096, 64, 256, 1 << 30
+    # one split per unit: 8 units of 8 heads per KV head, D floats + (m, l) each
+    assert g(B, Hkv * G, Hkv, D, L, L) == B * Hkv * 8 * 8 * (D * 4 + 8)
+    assert g(B, Hkv * G, Hkv, D, L, 16) == 0             # 2^26 splits per unit: > 2^64 bytes
+    assert h(B, 256, Hkv * G, Hkv, D, L, 16) == 0
+    assert g(1, 8, 2, 128, L, 16) == 2 * (L // 16) * 4 * (128 * 4 + 8)
 
 
 def test_batch_invariant_multi_and_ring_reject_bad_arguments(lib):
