@@ -3,12 +3,16 @@
 Each case draws a shape (head_dim, KV heads, group size, batch), ragged
 lengths (empty sequences included), windows, the cache layout (paged or
 contiguous, fp16 or int8 V) and an entry point: fa_decode, fa_decode_multi,
-fa_decode_ring and their batch-invariant forms.  A paged case outside the
-batch-invariant forms may take a block table of 2^20 tokens per sequence,
-which moves the planner to 16-column units when a KV head has more than 8
-columns; batches of many rows reach the warp-per-row merge.  Unwritten cache rows and the workspace hold NaN, so a
-read or weight of either shows up.
+fa_decode_ring and their batch-invariant forms.  Paged cases take pages of
+16, 32 or 64 tokens; a quarter of the single-query fa_decode and
+fa_decode_ring cases run on the CUDA-core split kernel (FA_DECODE_KERNEL=simt)
+instead of the tensor-core one.  A paged case outside the batch-invariant
+forms may take a block table of 2^20 tokens per sequence, which moves the
+planner to 16-column units when a KV head has more than 8 columns; batches of
+many rows reach the warp-per-row merge.  Unwritten cache rows and the
+workspace hold NaN, so a read or weight of either shows up.
 """
+import contextlib
 import os
 import zlib
 
@@ -48,8 +52,10 @@ def _draw(seed):
     big_cap = paged and not mode.endswith("_bi") and bool(r.random() < 0.6)
     tq = int(r.integers(2, 7)) if mode.startswith("multi") else 1
     split = int(r.choice([16, 64, 256, 512]))
+    P = int(r.choice([16, 16, 32, 64])) if paged else 16
+    simt = mode in ("decode", "ring") and bool(r.random() < 0.25)
     return dict(mode=mode, D=D, Hkv=Hkv, G=G, B=B, lens=lens, window=window, int8=int8,
-                paged=paged, big_cap=big_cap, tq=tq, split=split, seed=seed)
+                paged=paged, big_cap=big_cap, tq=tq, split=split, P=P, simt=simt, seed=seed)
 
 
 def _ws(n):
@@ -60,8 +66,8 @@ def _run_paged_or_contig(c):
     mode, D, Hkv, G, B, tq = c["mode"], c["D"], c["Hkv"], c["G"], c["B"], c["tq"]
     Hq = G * Hkv
     name = f"fuzz{c['seed']}"
-    wl = Workload(name, B, Hq, Hkv, D, paged=c["paged"], v_int8=c["int8"], window=c["window"],
-                  window_odd_only=c["seed"] % 2 == 1,
+    wl = Workload(name, B, Hq, Hkv, D, paged=c["paged"], page_size=c["P"], v_int8=c["int8"],
+                  window=c["window"], window_odd_only=c["seed"] % 2 == 1,
                   seed=20000 + zlib.crc32(name.encode()) % 1000)
     cap = max(max(c["lens"]), 1)
     if c["big_cap"]:
@@ -70,12 +76,13 @@ def _run_paged_or_contig(c):
         cap = -(-cap // 16) * 16
     inp = build_case(wl, seq_lens=c["lens"], capacity=cap, spare_blocks=2 if c["paged"] else 0)
     d = to_cuda(inp)
-    cap_tok = d["max_blocks"] * (16 if c["paged"] else 1)
-    kw = dict(max_blocks_per_seq=d["max_blocks"], num_blocks=d["num_blocks"] if c["paged"] else 0)
+    cap_tok = d["max_blocks"] * (c["P"] if c["paged"] else 1)
+    kw = dict(max_blocks_per_seq=d["max_blocks"], num_blocks=d["num_blocks"] if c["paged"] else 0,
+              page_size=c["P"])
     okw = dict(scale=wl.scale, n_kv_heads=Hkv,
                v_scales=None if not c["int8"] else inp["v_scales"].numpy(),
                block_table=None if not c["paged"] else inp["block_table"].numpy(),
-               window=None if inp["window"] is None else inp["window"].numpy(), page_size=16,
+               window=None if inp["window"] is None else inp["window"].numpy(), page_size=c["P"],
                max_blocks=inp["max_blocks"])
     if mode in ("decode", "decode_bi"):
         out = torch.full((B, Hq, D), float("nan"), device="cuda")
@@ -154,8 +161,26 @@ def _run_ring(c):
     return out.cpu().numpy(), want
 
 
+@contextlib.contextmanager
+def _split_kernel(simt):
+    """The library reads FA_DECODE_KERNEL at every call."""
+    old = os.environ.get("FA_DECODE_KERNEL")
+    if simt:
+        os.environ["FA_DECODE_KERNEL"] = "simt"
+    else:
+        os.environ.pop("FA_DECODE_KERNEL", None)
+    try:
+        yield
+    finally:
+        if old is None:
+            os.environ.pop("FA_DECODE_KERNEL", None)
+        else:
+            os.environ["FA_DECODE_KERNEL"] = old
+
+
 @pytest.mark.parametrize("seed", range(N_CASES))
 def test_random_case_matches_oracle(seed):
     c = _draw(seed)
-    got, want = (_run_ring if c["mode"].startswith("ring") else _run_paged_or_contig)(c)
+    with _split_kernel(c["simt"]):
+        got, want = (_run_ring if c["mode"].startswith("ring") else _run_paged_or_contig)(c)
     assert_close(got, want, c["int8"], str(c))
