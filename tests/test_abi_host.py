@@ -215,3 +215,30 @@ def test_batch_invariant_multi_and_ring_reject_bad_arguments(lib):
     assert h(1, 1, 8, 2, 128, 512, 512) == lib.fa_decode_batch_invariant_workspace_size(
         1, 8, 2, 128, 512, 512)
     assert h(1, 4, 8, 2, 128, 512, 512) == 2 * 2 * 1 * 8 * (128 * 4 + 8)
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    """No CPU or PyTorch fallback: without the built library (or with a build
+    that fails) the first call raises instead of computing anything."""
+    import subprocess
+    import sys
+    code = f"""
+import torch
+from decode_step_kv_gb300 import _build, binding
+_build.LIB = {str(tmp_path / "absent.so")!r}
+try:
+    binding.load(build_if_missing=False)
+except OSError:
+    print("absent: raised")
+def broken(*a, **k):
+    raise RuntimeError("nvcc failed")
+_build.build = broken
+try:
+    binding.fa_decode_workspace_size(1, 8, 2, 128, 512, 152)
+except RuntimeError as e:
+    print("build:", e)
+"""
+    r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, capture_output=True, text=True,
+                       timeout=300)
+    assert r.returncode == 0, r.stderr
+    assert "absent: raised" in r.stdout and "build: nvcc failed" in r.stdout, r.stdout
