@@ -471,22 +471,44 @@ def time_next_rows(steps, device, peak):
     return res
 
 
+def e2e_copies(wl, lens, host, dev):
+    """The host->device copies of one end-to-end step, as (destination,
+    source) pairs.  A contiguous cache ([B][Hkv][cap][...]) crosses as each
+    (sequence, KV head)'s written rows [0, L_b), which are contiguous on both
+    sides, not its whole capacity; a paged cache crosses as its whole block
+    pool; every other input whole."""
+    copies = []
+    for n, src in host.items():
+        if not wl.paged and n in ("k_cache", "v_cache", "v_scales"):
+            for b, L in enumerate(lens):
+                for kv in range(wl.n_kv_heads):
+                    if L > 0:
+                        copies.append((dev[n][b, kv, :L], src[b, kv, :L]))
+        else:
+            copies.append((dev[n], src))
+    return copies
+
+
 def time_e2e(wl, d, steps, warmup, device):
     """Same step through the public API with host inputs: pinned host -> device
-    copies of every input, fa_decode, device -> host copy of the output."""
+    copies of the step's inputs (e2e_copies), fa_decode, device -> host copy of
+    the output.  Also reports whether that output is bit-identical to the
+    resident step's."""
     import torch
     names = ["q", "k_cache", "v_cache", "v_scales", "block_table", "seq_lens", "window"]
     host = {n: d[n].cpu().pin_memory() for n in names if d.get(n) is not None}
     dev = {n: torch.empty_like(d[n]) for n in host}
+    copies = e2e_copies(wl, d["lens"], host, dev)
     out_h = torch.empty(d["out"].shape, dtype=torch.float32).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    h2d = sum(src.numel() * src.element_size() for _, src in copies)
     d2h = out_h.numel() * 4
     stream = torch.cuda.current_stream(device)
     dd = dict(d)
+    dd["out"] = torch.empty_like(d["out"])
 
     def step():
-        for n in host:
-            dev[n].copy_(host[n], non_blocking=True)
+        for dst, src in copies:
+            dst.copy_(src, non_blocking=True)
         dd.update(dev)
         call(wl, dd, stream)
         out_h.copy_(dd["out"], non_blocking=True)
@@ -502,7 +524,10 @@ def time_e2e(wl, d, steps, warmup, device):
         ev[i][1].record(stream)
     torch.cuda.synchronize(device)
     ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
-    return ms, h2d, d2h
+    call(wl, d, stream)                       # the resident step, same plan
+    torch.cuda.synchronize(device)
+    same = bool(torch.equal(out_h, d["out"].cpu()))
+    return ms, h2d, d2h, same
 
 
 def time_e2e_serving(wl, d, steps, warmup, device):
@@ -677,12 +702,14 @@ def run_ours(args, world, rank, local):
                           "note": "same steps back to back without the L2 flush (informative; "
                                   "the headline is cold L2)"}
     if not args.no_e2e:
-        ms, h2d, d2h = time_e2e(wl, d, max(5, args.steps // 5), 2, device)
+        ms, h2d, d2h, same = time_e2e(wl, d, max(5, args.steps // 5), 2, device)
         line["e2e"] = {"value": round(r["kv_bytes"] / (ms * 1e-3) / 1e9 * world, 2),
                        "unit": "GB/s", "us_per_step": round(ms * 1e3, 2),
                        "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                       "note": "every input, the whole KV cache included, copied host->device "
-                               "each step"}
+                       "output_equals_resident": same,
+                       "note": "every input copied host->device each step: a contiguous "
+                               "cache as each (sequence, kv head)'s written rows, a paged "
+                               "cache as its whole block pool"}
         ms2, h2d2, d2h2 = time_e2e_serving(wl, d, max(5, args.steps // 5), 2, device)
         line["e2e_serving"] = {"value": round(r["kv_bytes"] / (ms2 * 1e-3) / 1e9 * world, 2),
                                "unit": "GB/s", "us_per_step": round(ms2 * 1e3, 2),

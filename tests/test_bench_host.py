@@ -31,3 +31,39 @@ def test_traffic_is_read_only_for_the_source_it_was_taken_on(tmp_path, monkeypat
     assert bench.recorded_traffic("fa_stream_mma_kernel", "4x1k-8k_d256") is None
     assert bench.recorded_traffic("fa_stream_mma_kernel", "no_such_workload") is None
 
+
+
+def test_e2e_copies_send_written_rows_of_a_contiguous_cache():
+    """The end-to-end leg sends each (sequence, KV head)'s rows [0, L_b) of a
+    contiguous cache, at the same place on both sides, and everything else
+    whole; a paged pool goes whole."""
+    import dataclasses
+
+    import torch
+
+    from decode_step_kv_gb300.inputs import Workload
+    wl = Workload("t", 3, 4, 2, 128)
+    lens = [5, 0, 16]
+    cap = 16
+    host = {"q": torch.randn(3, 4, 128).half(),
+            "k_cache": torch.randn(3, 2, cap, 128).half(),
+            "v_cache": torch.randint(-127, 128, (3, 2, cap, 128), dtype=torch.int8),
+            "v_scales": torch.randn(3, 2, cap, 4).half(),
+            "seq_lens": torch.tensor(lens, dtype=torch.int32)}
+    dev = {n: torch.zeros_like(t) for n, t in host.items()}
+    copies = bench.e2e_copies(wl, lens, host, dev)
+    row = 128 * 2 + 128 + 4 * 2                  # K fp16 + V int8 + scales, per token
+    assert sum(s.numel() * s.element_size() for _, s in copies) == \
+        sum(lens) * 2 * row + 3 * 4 * 128 * 2 + 3 * 4
+    for dst, src in copies:
+        assert src.is_contiguous() and dst.is_contiguous()
+        dst.copy_(src)
+    for n in ("k_cache", "v_cache", "v_scales"):
+        for b, L in enumerate(lens):
+            assert torch.equal(dev[n][b, :, :L], host[n][b, :, :L])
+            assert not dev[n][b, :, L:].any()     # padding rows were not sent
+    paged = dataclasses.replace(wl, paged=True)
+    pool = {"k_cache": torch.randn(7, 2, 16, 128).half()}
+    assert [(d.shape, s.shape) for d, s in bench.e2e_copies(paged, lens, pool,
+                                                             {"k_cache": pool["k_cache"]})] == \
+        [(pool["k_cache"].shape, pool["k_cache"].shape)]
