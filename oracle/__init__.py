@@ -60,38 +60,42 @@ def build(force: bool = False) -> str:
     return _LIB_PATH
 
 
+def _configure(lib):
+    """Declare the C signatures on a loaded copy of the oracle library."""
+    P = ctypes.c_void_p
+    i32, i64, dbl = ctypes.c_int, ctypes.c_longlong, ctypes.c_double
+    lib.oracle_fa_decode.argtypes = [P, P, P, P, P, P, P, i32, i32, i32, i32, i32,
+                                     i32, dbl, P, i32, i32, P]
+    lib.oracle_fa_decode.restype = i32
+    lib.oracle_fa_weights.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32, i32,
+                                      dbl, i32, i32, P, P, P]
+    lib.oracle_fa_weights.restype = i32
+    lib.oracle_pack_v_int8.argtypes = [P, i64, i32, P, P]
+    lib.oracle_pack_v_int8.restype = i32
+    lib.oracle_gather_rows.argtypes = [P, i32, P, i32, i32, i32, i32, i32, P]
+    lib.oracle_gather_rows.restype = i32
+    lib.oracle_append_kv.argtypes = [P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32]
+    lib.oracle_append_kv.restype = i32
+    lib.oracle_fa_decode_ring.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, i32, dbl,
+                                          P, i32, i32, P]
+    lib.oracle_fa_decode_ring.restype = i32
+    lib.oracle_fa_decode_multi.argtypes = [P, P, P, P, P, P, P, i32, i32, i32, i32, i32,
+                                           i32, i32, dbl, P, i32, i32, P]
+    lib.oracle_fa_decode_multi.restype = i32
+    lib.oracle_append_kv_ring.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32]
+    lib.oracle_append_kv_ring.restype = i32
+    lib.oracle_half_to_double.argtypes = [ctypes.c_uint16]
+    lib.oracle_half_to_double.restype = dbl
+    lib.oracle_double_to_half.argtypes = [dbl]
+    lib.oracle_double_to_half.restype = ctypes.c_uint16
+    return lib
+
+
 def _load():
     global _lib
     with _lock:
         if _lib is None:
-            lib = ctypes.CDLL(build())
-            P = ctypes.c_void_p
-            i32, i64, dbl = ctypes.c_int, ctypes.c_longlong, ctypes.c_double
-            lib.oracle_fa_decode.argtypes = [P, P, P, P, P, P, P, i32, i32, i32, i32, i32,
-                                             i32, dbl, P, i32, i32, P]
-            lib.oracle_fa_decode.restype = i32
-            lib.oracle_fa_weights.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32, i32,
-                                              dbl, i32, i32, P, P, P]
-            lib.oracle_fa_weights.restype = i32
-            lib.oracle_pack_v_int8.argtypes = [P, i64, i32, P, P]
-            lib.oracle_pack_v_int8.restype = i32
-            lib.oracle_gather_rows.argtypes = [P, i32, P, i32, i32, i32, i32, i32, P]
-            lib.oracle_gather_rows.restype = i32
-            lib.oracle_append_kv.argtypes = [P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32]
-            lib.oracle_append_kv.restype = i32
-            lib.oracle_fa_decode_ring.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, i32, dbl,
-                                                  P, i32, i32, P]
-            lib.oracle_fa_decode_ring.restype = i32
-            lib.oracle_fa_decode_multi.argtypes = [P, P, P, P, P, P, P, i32, i32, i32, i32, i32,
-                                                   i32, i32, dbl, P, i32, i32, P]
-            lib.oracle_fa_decode_multi.restype = i32
-            lib.oracle_append_kv_ring.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32]
-            lib.oracle_append_kv_ring.restype = i32
-            lib.oracle_half_to_double.argtypes = [ctypes.c_uint16]
-            lib.oracle_half_to_double.restype = dbl
-            lib.oracle_double_to_half.argtypes = [dbl]
-            lib.oracle_double_to_half.restype = ctypes.c_uint16
-            _lib = lib
+            _lib = _configure(ctypes.CDLL(build()))
     return _lib
 
 
