@@ -67,3 +67,23 @@ def test_e2e_copies_send_written_rows_of_a_contiguous_cache():
     assert [(d.shape, s.shape) for d, s in bench.e2e_copies(paged, lens, pool,
                                                              {"k_cache": pool["k_cache"]})] == \
         [(pool["k_cache"].shape, pool["k_cache"].shape)]
+
+
+def test_clock_summary_reads_median_max_and_active_reasons():
+    """nvidia-smi csv,noheader,nounits lines -> median SM clock, max clock
+    and the throttle reasons seen Active; malformed lines are skipped."""
+    s = bench.ClockSampler(0)
+    s.lines = [
+        "0, 2070, 2070, 900.10, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active",
+        "0, 1980, 2070, 1390.00, 0x0000000000000004, Not Active, Not Active, Not Active, Active",
+        "0, 2070, 2070, 1100.00, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active",
+        "garbage",
+        "0, [N/A], 2070, 1.0, 0x0, Active, Active, Active, Active",
+    ]
+    got = s.summary()
+    assert got == {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"],
+                   "samples": 3}
+    s.lines = ["0, 1500, 2070, 500.0, 0x8, Not Active, Active, Not Active, Not Active"]
+    assert s.summary()["reasons"] == ["hw_thermal_slowdown"]
+    s.lines = []
+    assert s.summary() is None
