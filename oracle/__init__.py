@@ -23,11 +23,14 @@ C source; in short:
 * ``decode_multi`` -- several query tokens per sequence (speculative
   verify), each attending causally up to its own position;
 * ``decode_ring`` / ``append_kv_ring`` -- the same over a ring cache (token t
-  at row t % capacity, only the last `capacity` tokens attended).
+  at row t % capacity, only the last `capacity` tokens attended);
+* ``decode_slots`` / ``append_kv_slots`` -- row b uses cache slot
+  ``slot_ids[b]`` of a pool of per-slot contiguous or ring caches (the slot
+  map the batched kernels of "flash_attn_vec_hybrid.metal" read per row).
 
 Every function here is pinned by ``tests/test_oracle_pins.py``,
-``tests/test_oracle_append.py``, ``tests/test_oracle_ring.py`` and
-``tests/test_oracle_multi.py``.
+``tests/test_oracle_append.py``, ``tests/test_oracle_ring.py``,
+``tests/test_oracle_multi.py`` and ``tests/test_oracle_slots.py``.
 """
 from __future__ import annotations
 
@@ -84,6 +87,11 @@ def _configure(lib):
     lib.oracle_fa_decode_multi.restype = i32
     lib.oracle_append_kv_ring.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32]
     lib.oracle_append_kv_ring.restype = i32
+    lib.oracle_fa_decode_slots.argtypes = [P, P, P, P, P, i32, P, P, i32, i32, i32, i32, i32,
+                                           i32, dbl, P, i32, i32, P]
+    lib.oracle_fa_decode_slots.restype = i32
+    lib.oracle_append_kv_slots.argtypes = [P, P, P, P, P, P, i32, P, i32, i32, i32, i32, i32]
+    lib.oracle_append_kv_slots.restype = i32
     lib.oracle_half_to_double.argtypes = [ctypes.c_uint16]
     lib.oracle_half_to_double.restype = dbl
     lib.oracle_double_to_half.argtypes = [dbl]
@@ -222,6 +230,67 @@ def decode_ring(q, k_cache, v_cache, seq_lens, *, scale, n_kv_heads, v_scales=No
     if rc:
         raise OracleError(f"oracle_fa_decode_ring returned {rc}")
     return out.reshape(B, Hq, D) if rows is None else out
+
+
+def decode_slots(q, k_cache, v_cache, seq_lens, slot_ids, *, scale, n_kv_heads, v_scales=None,
+                 window=None, ring=False, rows=None, threads=0):
+    """Oracle output when row b uses cache slot slot_ids[b] of a pool
+    [n_slots, Hkv, capacity, D] of contiguous (ring=False) or ring (ring=True)
+    slots; q / seq_lens / window / the output are per row.  A slot id outside
+    [0, n_slots) gives a zero row."""
+    lib = _load()
+    qb = _half_bits(q)
+    B, Hq, D = qb.shape
+    kb = _half_bits(k_cache)
+    n_slots, cap = kb.shape[0], kb.shape[2]
+    if v_scales is None:
+        vb, sb = _half_bits(v_cache), None
+    else:
+        vb, sb = _c(v_cache, np.int8), _half_bits(v_scales)
+    sl = _c(np.asarray(seq_lens, dtype=np.int32), np.int32)
+    si = _c(np.asarray(slot_ids, dtype=np.int32), np.int32)
+    wn = None if window is None else _c(np.asarray(window, dtype=np.int32), np.int32)
+    if rows is None:
+        rr, n = None, B * Hq
+    else:
+        rr = _c(np.asarray(rows, dtype=np.int32), np.int32)
+        n = rr.size
+    out = np.zeros((n, D), dtype=np.float64)
+    rc = lib.oracle_fa_decode_slots(_ptr(qb), _ptr(kb), _ptr(vb), _ptr(sb), _ptr(si),
+                                    int(n_slots), _ptr(sl), _ptr(wn), B, Hq, int(n_kv_heads), D,
+                                    int(cap), int(bool(ring)), float(scale), _ptr(rr), n,
+                                    int(threads), _ptr(out))
+    if rc:
+        raise OracleError(f"oracle_fa_decode_slots returned {rc}")
+    return out.reshape(B, Hq, D) if rows is None else out
+
+
+def append_kv_slots(k_new, v_new, k_cache, v_cache, slot_ids, positions, *, v_scales=None,
+                    ring=False):
+    """append_kv into a pool of per-slot caches [n_slots, Hkv, capacity, ...]:
+    row b writes slot slot_ids[b] at positions[b] (row positions[b] % capacity
+    for a ring).  Returns new (k_cache, v_cache, v_scales) arrays."""
+    lib = _load()
+    kn = _c(np.asarray(k_new, dtype=np.float32), np.float32)
+    vn = _c(np.asarray(v_new, dtype=np.float32), np.float32)
+    B, Hkv, D = kn.shape
+    kc = np.array(k_cache, copy=True).view(np.uint16)
+    vc = np.array(v_cache, copy=True)
+    sc = None
+    if v_scales is None:
+        vc = vc.view(np.uint16)
+    else:
+        sc = np.array(v_scales, copy=True).view(np.uint16)
+    si = _c(np.asarray(slot_ids, dtype=np.int32), np.int32)
+    pos = _c(np.asarray(positions, dtype=np.int32), np.int32)
+    rc = lib.oracle_append_kv_slots(_ptr(kn), _ptr(vn), _ptr(kc), _ptr(vc), _ptr(sc), _ptr(si),
+                                    int(kc.shape[0]), _ptr(pos), B, Hkv, D, int(kc.shape[2]),
+                                    int(bool(ring)))
+    if rc:
+        raise OracleError(f"oracle_append_kv_slots returned {rc}")
+    if sc is None:
+        return kc.view(np.float16), vc.view(np.float16), None
+    return kc.view(np.float16), vc, sc.view(np.float16)
 
 
 def append_kv_ring(k_new, v_new, k_cache, v_cache, positions, *, v_scales=None):

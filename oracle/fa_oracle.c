@@ -26,6 +26,9 @@
  *   - an empty range gives 0 ("S == 0 ? 0" in the output write).
  *   The cache append (oracle_append_kv, at the end) writes one step's K and V
  *   rows at each sequence's position.
+ *   A slot map (oracle_fa_decode_slots, oracle_append_kv_slots) lets row b
+ *   use cache slot slot_ids[b] of a pool of per-slot caches, as the batched
+ *   kernels of the same page read slot_id_arr per query row.
  *   The int8 V codec (int8 codes times one fp16 scale per 32 elements) follows
  *   ggml's block_q8_0 dequantisation (qs[i] * d) shown on the DS4Server page
  *   "dsv4_hc.metal"; the quantiser itself (amax / 127, round half to even,
@@ -138,7 +141,19 @@ typedef struct {
     double scale;
     int ring;                  /* contiguous ring cache: token t at row t % capacity */
     int tq;                    /* queries per sequence (q is [B][tq][Hq][D]); 0 or 1 = one */
+    const int32_t *slot_ids;   /* contiguous only: row b's cache is slot slot_ids[b] of
+                                  [n_slots][Hkv][cap][D]; NULL => slot b */
+    int n_slots;
 } oracle_problem;
+
+/* Cache slot of row b, or -1 when its slot id names no slot. */
+static long long slot_of(const oracle_problem *P, int b)
+{
+    if (!P->slot_ids)
+        return b;
+    long long s = P->slot_ids[b];
+    return (s >= 0 && s < P->n_slots) ? s : -1;
+}
 
 /* Element offset of row (b, kv, t) in a cache whose rows hold `row_elems`. */
 static long long row_offset(const oracle_problem *P, int b, int kv, int t,
@@ -152,7 +167,7 @@ static long long row_offset(const oracle_problem *P, int b, int kv, int t,
     /* contiguous: capacity (tokens) = max_blocks; a ring cache keeps token t
      * at row t % capacity */
     long long r = P->ring ? t % P->max_blocks : t;
-    return (((long long)b * P->Hkv + kv) * P->max_blocks + r) * (long long)row_elems;
+    return ((slot_of(P, b) * P->Hkv + kv) * P->max_blocks + r) * (long long)row_elems;
 }
 
 static double v_elem(const oracle_problem *P, int b, int kv, int t, int d)
@@ -187,6 +202,9 @@ static void attended_range(const oracle_problem *P, int b, int j, int *lo, int *
      * length min(seq_pos + 1, capacity) of the ring storage mode) */
     if (P->ring && *hi - P->max_blocks > *lo)
         *lo = *hi - P->max_blocks;
+    /* a slot id that names no slot: no cache, an empty range */
+    if (slot_of(P, b) < 0)
+        *lo = *hi = 0;
 }
 
 /* Softmax weights p_t, t in [lo, hi), of row (b, h).  p must hold hi-lo. */
@@ -276,6 +294,8 @@ static int validate(const oracle_problem *P)
                                    : (long long)P->max_blocks;
     if (P->ring && (P->block_table || P->max_blocks <= 0))
         return -6;
+    if (P->slot_ids && (P->block_table || P->n_slots <= 0 || P->max_blocks <= 0))
+        return -6;
     for (int b = 0; b < P->B; ++b)
         if (P->seq_lens[b] < 0 || (!P->ring && P->seq_lens[b] > cap))
             return -6;
@@ -337,6 +357,30 @@ int oracle_fa_decode_ring(const uint16_t *q, const uint16_t *k_cache, const void
 {
     oracle_problem P = {q, k_cache, v_cache, v_scales, NULL, seq_lens, window,
                         B, Hq, Hkv, D, 1, capacity, scale, 1, 1};
+    return decode_impl(&P, rows, n_rows, n_threads, out);
+}
+
+/*
+ * Decode over a pool of per-slot caches addressed through a slot map: the
+ * batched kernels of the mlx-native page read, per query row, the row's cache
+ * slot (slot_id_arr) and position (seq_pos_arr) on the device, and address
+ * the K/V rows of that slot in a [slots][n_kv_heads][capacity][head_dim]
+ * pool.  Here row b of q, seq_lens, window and out uses slot slot_ids[b] of
+ * k_cache / v_cache / v_scales [n_slots][Hkv][capacity][...]; seq_lens[b] is
+ * that slot's length (the page's seq_pos + 1).  ring = 0: plain contiguous
+ * slots (seq_lens[b] <= capacity); ring = 1: each slot a ring as in
+ * oracle_fa_decode_ring.  A slot id outside [0, n_slots) gives a zero row.
+ */
+int oracle_fa_decode_slots(const uint16_t *q, const uint16_t *k_cache, const void *v_cache,
+                           const uint16_t *v_scales, const int32_t *slot_ids, int n_slots,
+                           const int32_t *seq_lens, const int32_t *window, int B, int Hq,
+                           int Hkv, int D, int capacity, int ring, double scale,
+                           const int32_t *rows, int n_rows, int n_threads, double *out)
+{
+    if (!slot_ids)
+        return -1;
+    oracle_problem P = {q, k_cache, v_cache, v_scales, NULL, seq_lens, window,
+                        B, Hq, Hkv, D, 1, capacity, scale, ring ? 1 : 0, 1, slot_ids, n_slots};
     return decode_impl(&P, rows, n_rows, n_threads, out);
 }
 
@@ -440,14 +484,14 @@ int oracle_gather_rows(const void *cache, int row_bytes, const int32_t *block_ta
 static int append_impl(const float *k_new, const float *v_new, uint16_t *k_cache, void *v_cache,
                        uint16_t *v_scales, const int32_t *block_table, const int32_t *positions,
                        int B, int Hkv, int D, int page_size, int max_blocks, int num_blocks,
-                       int ring);
+                       int ring, const int32_t *slot_ids, int n_slots);
 
 int oracle_append_kv(const float *k_new, const float *v_new, uint16_t *k_cache, void *v_cache,
                      uint16_t *v_scales, const int32_t *block_table, const int32_t *positions,
                      int B, int Hkv, int D, int page_size, int max_blocks, int num_blocks)
 {
     return append_impl(k_new, v_new, k_cache, v_cache, v_scales, block_table, positions, B, Hkv,
-                       D, page_size, max_blocks, num_blocks, 0);
+                       D, page_size, max_blocks, num_blocks, 0, NULL, 0);
 }
 
 /* Append into a ring cache: token t goes to row t % capacity (t >= 0). */
@@ -456,13 +500,29 @@ int oracle_append_kv_ring(const float *k_new, const float *v_new, uint16_t *k_ca
                           int Hkv, int D, int capacity)
 {
     return append_impl(k_new, v_new, k_cache, v_cache, v_scales, NULL, positions, B, Hkv, D, 1,
-                       capacity, 0, 1);
+                       capacity, 0, 1, NULL, 0);
+}
+
+/* Append into a pool of per-slot caches [n_slots][Hkv][capacity][...]: row b
+ * of k_new / v_new / positions writes slot slot_ids[b] (the slot map of
+ * oracle_fa_decode_slots), as a plain contiguous slot (ring = 0) or a ring
+ * (ring = 1).  A slot id outside [0, n_slots) writes nothing.  Rows are
+ * written in order b = 0, 1, ... */
+int oracle_append_kv_slots(const float *k_new, const float *v_new, uint16_t *k_cache,
+                           void *v_cache, uint16_t *v_scales, const int32_t *slot_ids,
+                           int n_slots, const int32_t *positions, int B, int Hkv, int D,
+                           int capacity, int ring)
+{
+    if (!slot_ids || n_slots <= 0 || capacity <= 0)
+        return -6;
+    return append_impl(k_new, v_new, k_cache, v_cache, v_scales, NULL, positions, B, Hkv, D, 1,
+                       capacity, 0, ring ? 1 : 0, slot_ids, n_slots);
 }
 
 static int append_impl(const float *k_new, const float *v_new, uint16_t *k_cache, void *v_cache,
                        uint16_t *v_scales, const int32_t *block_table, const int32_t *positions,
                        int B, int Hkv, int D, int page_size, int max_blocks, int num_blocks,
-                       int ring)
+                       int ring, const int32_t *slot_ids, int n_slots)
 {
     if (!k_new || !v_new || !k_cache || !v_cache || !positions || B < 0 || Hkv <= 0 || D <= 0)
         return -1;
@@ -477,6 +537,12 @@ static int append_impl(const float *k_new, const float *v_new, uint16_t *k_cache
             continue;
         if (ring)
             t %= cap;
+        long long slot = b;
+        if (slot_ids) {
+            slot = slot_ids[b];
+            if (slot < 0 || slot >= n_slots)
+                continue;
+        }
         for (int kv = 0; kv < Hkv; ++kv) {
             long long row;
             if (block_table) {
@@ -485,7 +551,7 @@ static int append_impl(const float *k_new, const float *v_new, uint16_t *k_cache
                     continue;
                 row = (blk * Hkv + kv) * page_size + t % page_size;
             } else {
-                row = ((long long)b * Hkv + kv) * max_blocks + t;
+                row = (slot * Hkv + kv) * max_blocks + t;
             }
             const float *kr = k_new + ((long long)b * Hkv + kv) * D;
             const float *vr = v_new + ((long long)b * Hkv + kv) * D;

@@ -20,7 +20,8 @@ import oracle
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 SRC = os.path.join(ROOT, "oracle", "fa_oracle.c")
-PIN_MODULES = ["test_oracle_pins", "test_oracle_multi", "test_oracle_ring", "test_oracle_append"]
+PIN_MODULES = ["test_oracle_pins", "test_oracle_multi", "test_oracle_ring", "test_oracle_append",
+               "test_oracle_slots"]
 
 # (name, text in fa_oracle.c, replacement); the text must occur in the file
 MUTANTS = [
@@ -66,8 +67,13 @@ MUTANTS = [
      "k_cache[row * D + d] = oracle_double_to_half((double)kr[d]);",
      "k_cache[row * D + d] = oracle_double_to_half((double)vr[d]);"),
     ("append to the next contiguous row",
-     "row = ((long long)b * Hkv + kv) * max_blocks + t;",
-     "row = ((long long)b * Hkv + kv) * max_blocks + (t + 1) % max_blocks;"),
+     "row = (slot * Hkv + kv) * max_blocks + t;",
+     "row = (slot * Hkv + kv) * max_blocks + (t + 1) % max_blocks;"),
+    ("slot map ignored: row b reads slot b",
+     "return ((slot_of(P, b) * P->Hkv + kv) * P->max_blocks + r) * (long long)row_elems;",
+     "return (((long long)b * P->Hkv + kv) * P->max_blocks + r) * (long long)row_elems;"),
+    ("append through the slot map writes slot b",
+     "            slot = slot_ids[b];\n", "            slot = b;\n"),
     ("gather reads the row after",
      "off = ((blk * Hkv + kv) * page_size + t % page_size) * (long long)row_bytes;",
      "off = ((blk * Hkv + kv) * page_size + (t + 1) % page_size) * (long long)row_bytes;"),
