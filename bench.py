@@ -3,9 +3,10 @@
 
 One step = one fa_decode call (split-K kernel + log-sum-exp merge kernel)
 over every sequence of the workload, inputs resident in HBM.  The headline
-line is measured on the 4-sequence, 16/8-head, head_dim 256, ragged
-1K-8K workload (4x1k-8k_d256); every other decode workload is measured too and
-listed under "configs".
+line is measured on the largest decode workload that fits one GPU: 32
+sequences of 32K keys, 32 query / 8 KV heads, head_dim 128, paged fp16
+K/V (32x32k_d128_paged, 4.29 GB of K/V per step); every decode workload,
+that one included, is measured too and listed under "configs".
 
 Timing: W untimed warm-up steps, then K timed steps bracketed by a barrier and
 torch.cuda.synchronize() on both sides; each step is timed with CUDA events on
@@ -38,7 +39,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "decode attention µs/step and KV-read GB/s (fraction of GB300 HBM peak)"
-HEADLINE = "4x1k-8k_d256"
+HEADLINE = "32x32k_d128_paged"
 L2_BYTES = 129 * 2 ** 20
 FALLBACK_HBM_GBS = 6800.0
 

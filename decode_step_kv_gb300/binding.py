@@ -22,6 +22,7 @@ FA_STATUS_LEN_CLAMPED = 1
 FA_STATUS_BAD_BLOCK = 2
 FA_STATUS_WAIT_TIMEOUT = 4
 FA_STATUS_POS_RANGE = 8
+FA_STATUS_BAD_SLOT = 16
 
 
 class FaDecodeError(RuntimeError):
@@ -74,6 +75,12 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
             lib.fa_decode_ring.restype = i32
             lib.fa_append_kv_ring.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, P]
             lib.fa_append_kv_ring.restype = i32
+            lib.fa_decode_slots.argtypes = [P, P, P, P, P, P, i32, i32, i32, f32, P, P, i32, i32,
+                                            i32, i32, P, sz, P]
+            lib.fa_decode_slots.restype = i32
+            lib.fa_append_kv_slots.argtypes = [P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32,
+                                               P]
+            lib.fa_append_kv_slots.restype = i32
             lib.fa_append_kv.argtypes = [P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, P]
             lib.fa_append_kv.restype = i32
             lib.fa_gather_kv_debug.argtypes = [P, i32, P, i32, i32, i32, i32, i32, i32, P, P]
@@ -251,6 +258,31 @@ def fa_append_kv_ring(k_new, v_new, k_cache, v_cache, v_scales, positions, *, st
                                   _ptr(v_scales), _ptr(positions), int(k_new.shape[0]),
                                   int(k_new.shape[1]), int(k_new.shape[2]),
                                   int(k_cache.shape[2]), _stream(stream))
+    _check(rc)
+
+
+def fa_decode_slots(q, k_cache, v_cache, v_scales, slot_ids, seq_lens, n_q_heads, n_kv_heads,
+                    head_dim, scale, window, out, *, ring=False, workspace=None, stream=None):
+    """Decode where row b reads slot slot_ids[b] of a pool [n_slots, Hkv, capacity, D]
+    of contiguous (ring=False) or ring (ring=True) caches."""
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = load().fa_decode_slots(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(v_scales),
+                                _ptr(slot_ids), _ptr(seq_lens), int(n_q_heads), int(n_kv_heads),
+                                int(head_dim), float(scale), _ptr(window), _ptr(out),
+                                int(q.shape[0]), int(k_cache.shape[0]), int(k_cache.shape[2]),
+                                int(bool(ring)), _ptr(workspace), ws_bytes, _stream(stream))
+    _check(rc)
+
+
+def fa_append_kv_slots(k_new, v_new, k_cache, v_cache, v_scales, slot_ids, positions, *,
+                       ring=False, stream=None):
+    """Write row b's K / V into slot slot_ids[b] of a pool [n_slots, Hkv, capacity, D]
+    at token positions[b] (row positions[b] % capacity for a ring)."""
+    rc = load().fa_append_kv_slots(_ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
+                                   _ptr(v_scales), _ptr(slot_ids), _ptr(positions),
+                                   int(k_new.shape[0]), int(k_new.shape[1]), int(k_new.shape[2]),
+                                   int(k_cache.shape[0]), int(k_cache.shape[2]), int(bool(ring)),
+                                   _stream(stream))
     _check(rc)
 
 

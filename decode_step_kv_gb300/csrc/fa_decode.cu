@@ -50,6 +50,7 @@
 #include <string.h>
 
 #include <mutex>
+#include <utility>
 #include <stdlib.h>
 
 #include "../../include/fa_decode.h"
@@ -108,6 +109,9 @@ struct Params {
     int cpu;          // tensor-core kernel: (query, head) columns per unit, 8 or 16
     int chunk;        // batch-invariant plan: tiles per chunk (0: stream-K plan)
     int max_chunks;   // batch-invariant plan: chunk slots per unit
+    const int *slot;  // contiguous / ring caches: sequence b's cache is slot slot[b] of
+                      // [n_slots][Hkv][cap][D]; NULL: slot b
+    int n_slots;
 };
 
 // ------------------------------------------------------------ PTX wrappers
@@ -211,6 +215,21 @@ __device__ __forceinline__ void attended_range(const Params &p, int b, int &lo, 
     // a ring cache holds only the last cap tokens (live length min(N, cap))
     if (p.ring && (long long)hi - p.cap > lo)
         lo = static_cast<int>(hi - p.cap);
+    // a slot id that names no cache slot: nothing to attend (a zero row)
+    if (p.slot) {
+        const int s = p.slot[b];
+        if (s < 0 || s >= p.n_slots) {
+            if (report)
+                flag(FA_STATUS_BAD_SLOT);
+            lo = hi = 0;
+        }
+    }
+}
+
+// Cache slot of sequence b in a contiguous or ring cache (the slot map, or b).
+__device__ __forceinline__ long long cache_slot(const Params &p, int b)
+{
+    return p.slot ? p.slot[b] : b;
 }
 
 template <int TILE>
@@ -231,7 +250,7 @@ __device__ __forceinline__ long long row_offset(const Params &p, int b, int kv, 
         return ((blk * p.Hkv + kv) * p.page_size + tok % p.page_size) * (long long)row_bytes;
     }
     const long long r = p.ring ? tok % p.cap : tok;
-    return (((long long)b * p.Hkv + kv) * p.cap + r) * (long long)row_bytes;
+    return ((cache_slot(p, b) * p.Hkv + kv) * p.cap + r) * (long long)row_bytes;
 }
 
 // ------------------------------------------------------------- reductions
@@ -799,7 +818,7 @@ __device__ __forceinline__ long long tile_row(const Params &p, int b, int kv, in
             return -1;
         return (blk * p.Hkv + kv) * p.page_size + tok % p.page_size;
     }
-    return ((long long)b * p.Hkv + kv) * p.cap + (p.ring ? tok % p.cap : tok);
+    return (cache_slot(p, b) * p.Hkv + kv) * p.cap + (p.ring ? tok % p.cap : tok);
 }
 
 // Per-sequence walk over the flattened tile space.  Units (one KV head and
@@ -2003,7 +2022,13 @@ __global__ void fa_append_kernel(const Params p, const float *k_new, const float
         }
         row = (blk * p.Hkv + kv) * p.page_size + t % p.page_size;
     } else {
-        row = ((long long)b * p.Hkv + kv) * p.cap + t;
+        const long long sl = cache_slot(p, b);
+        if (sl < 0 || sl >= p.n_slots) {       // n_slots = batch without a slot map
+            if (threadIdx.x == 0 && kv == 0)
+                flag(FA_STATUS_BAD_SLOT);
+            return;
+        }
+        row = (sl * p.Hkv + kv) * p.cap + t;
     }
     const float *kr = k_new + ((long long)b * p.Hkv + kv) * D;
     const float *vr = v_new + ((long long)b * p.Hkv + kv) * D;
@@ -2128,6 +2153,11 @@ static Path choose_path()
 // K/V bytes (at full capacity) from which units of 16 columns are used: four
 // times GB300's 126.5 MiB L2.
 constexpr double TWO_GROUP_MIN_KV_BYTES = 512.0 * (1 << 20);
+// stream-K grid no larger than the capacity's tile bound allows (1), or one
+// full persistent wave whatever the step (0)
+#ifndef FA_GRID_CAP
+#define FA_GRID_CAP 1
+#endif
 
 static Plan make_plan(Path path, int B, int Hq, int Hkv, int D, long long cap, int num_sms,
                       bool vi8, int tq = 1, int chunk = 0)
@@ -2166,6 +2196,17 @@ static Plan make_plan(Path path, int B, int Hq, int Hkv, int D, long long cap, i
             cps = vi8 ? tc::Cfg<256, true>::CTAS_PER_SM : tc::Cfg<256, false>::CTAS_PER_SM;
         }
         pl.ctas = (num_sms > 0 ? num_sms : 1) * cps;
+        if (chunk == 0 && FA_GRID_CAP) {
+            // no more workers than the capacity can give MIN_TPW tiles each: a
+            // step's tiles are at most batch x units x ceil(capacity / 16),
+            // so a small step launches only the CTAs it can use (the device
+            // plan still sizes itself from the real lengths)
+            const long long max_t = (long long)B * pl.units * ((cap + tc::TILE - 1) / tc::TILE);
+            const long long w_cap = (max_t + tc::MIN_TPW - 1) / tc::MIN_TPW;
+            const long long c_cap = (w_cap + nw - 1) / nw;
+            if (c_cap < pl.ctas)
+                pl.ctas = static_cast<int>(c_cap > 0 ? c_cap : 1);
+        }
         pl.W = pl.ctas * nw;
         pl.tps = 0;
         pl.max_splits = 0;
@@ -2390,27 +2431,67 @@ static bool aligned_to(const void *x, unsigned bytes)
 // host-side name as a device address; noalloc_scratch() returns the real one.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[FA_NOALLOC_SCRATCH_BYTES];
 
-// Device address of g_noalloc_scratch on the current device, looked up once
-// per device (with that device current) and cached.
+// Unique id of the calling thread's current CUDA context, 0 when none is
+// current (driver entry points through the runtime, so no -lcuda).  Ids are
+// never reused within a process, unlike context handles.
+static unsigned long long current_ctx_id()
+{
+    static const auto fns = [] {
+        void *cur = nullptr, *id = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &cur, 4000, cudaEnableDefault,
+                                             &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            cur = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &id, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            id = nullptr;
+        return std::make_pair(reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(cur),
+                              reinterpret_cast<PFN_cuCtxGetId_v12000>(id));
+    }();
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (!fns.first || !fns.second || fns.first(&ctx) != CUDA_SUCCESS || !ctx ||
+        fns.second(ctx, &id) != CUDA_SUCCESS)
+        return 0;
+    return id;
+}
+
+// Device address of g_noalloc_scratch in the current context, looked up once
+// per context (with it current) and cached under the context's id, so a new
+// context on the same device (after cudaDeviceReset, or a caller's own
+// driver-API context) gets its own address.
 static int noalloc_scratch(void **out)
 {
     static std::mutex mu;
-    static void *cache[64] = {nullptr};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess)
-        return fail(FA_ERR_CUDA, "fa_decode_noalloc: cudaGetDevice failed");
+    constexpr int N = 64;
+    static unsigned long long ids[N];
+    static void *ptrs[N];
+    static int used = 0, next = 0;
+    unsigned long long id = current_ctx_id();
     std::lock_guard<std::mutex> lock(mu);
-    if (dev < 64 && cache[dev]) {
-        *out = cache[dev];
-        return 0;
-    }
+    if (id)
+        for (int i = 0; i < used; ++i)
+            if (ids[i] == id) {
+                *out = ptrs[i];
+                return 0;
+            }
     void *ptr = nullptr;
     const cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
-    if (e != cudaSuccess || !ptr)
+    if (e != cudaSuccess || !ptr) {
+        int dev = -1;
+        cudaGetDevice(&dev);
         return fail(FA_ERR_CUDA, "fa_decode_noalloc: cannot find the scratch array on device %d: %s",
                     dev, cudaGetErrorString(e));
-    if (dev < 64)
-        cache[dev] = ptr;
+    }
+    if (!id)
+        id = current_ctx_id();   // the lookup made the device's primary context current
+    if (id) {
+        const int slot = used < N ? used++ : (next++ % N);
+        ids[slot] = id;
+        ptrs[slot] = ptr;
+    }
     *out = ptr;
     return 0;
 }
@@ -2454,7 +2535,7 @@ static int decode_impl(const void *q, const void *k_cache, const void *v_cache,
                        float scale, const int32_t *window, void *out, int batch, int page_size,
                        int max_blocks_per_seq, int num_blocks, void *workspace,
                        size_t workspace_bytes, void *stream, bool ring, int tq,
-                       int chunk = 0);
+                       int chunk = 0, const int32_t *slot_ids = nullptr, int n_slots = 0);
 
 FA_API int fa_decode(const void *q, const void *k_cache, const void *v_cache,
                      const void *v_scales, const int32_t *block_table,
@@ -2616,12 +2697,31 @@ FA_API int fa_decode_ring(const void *q, const void *k_cache, const void *v_cach
                        workspace_bytes, stream, true, 1);
 }
 
+FA_API int fa_decode_slots(const void *q, const void *k_cache, const void *v_cache,
+                           const void *v_scales, const int32_t *slot_ids,
+                           const int32_t *seq_lens, int n_q_heads, int n_kv_heads, int head_dim,
+                           float scale, const int32_t *window, void *out, int batch, int n_slots,
+                           int capacity, int ring, void *workspace, size_t workspace_bytes,
+                           void *stream)
+{
+    g_err[0] = 0;
+    if (!slot_ids)
+        return fail(FA_ERR_NULL, "fa_decode_slots: slot_ids is required");
+    if (n_slots <= 0 || capacity <= 0 || (ring && capacity % 16))
+        return fail(FA_ERR_LAYOUT, "fa_decode_slots: n_slots %d and capacity %d must be positive "
+                                   "(capacity a multiple of 16 for a ring)", n_slots, capacity);
+    return decode_impl(q, k_cache, v_cache, v_scales, nullptr, seq_lens, n_q_heads, n_kv_heads,
+                       head_dim, scale, window, out, batch, 16, capacity, 0, workspace,
+                       workspace_bytes, stream, ring != 0, 1, 0, slot_ids, n_slots);
+}
+
 static int decode_impl(const void *q, const void *k_cache, const void *v_cache,
                        const void *v_scales, const int32_t *block_table,
                        const int32_t *seq_lens, int n_q_heads, int n_kv_heads, int head_dim,
                        float scale, const int32_t *window, void *out, int batch, int page_size,
                        int max_blocks_per_seq, int num_blocks, void *workspace,
-                       size_t workspace_bytes, void *stream, bool ring, int tq, int chunk)
+                       size_t workspace_bytes, void *stream, bool ring, int tq, int chunk,
+                       const int32_t *slot_ids, int n_slots)
 {
     g_err[0] = 0;
     if (!q || !k_cache || !v_cache || !seq_lens || !out)
@@ -2654,17 +2754,23 @@ static int decode_impl(const void *q, const void *k_cache, const void *v_cache,
     }
     if (cap > (1ll << 30))
         return fail(FA_ERR_LAYOUT, "fa_decode: capacity %lld tokens too large", cap);
+    if (slot_ids && (n_slots <= 0 || (double)n_slots * n_kv_heads * (double)cap > 1e15))
+        return fail(FA_ERR_LAYOUT, "fa_decode: bad slot count %d for capacity %lld", n_slots, cap);
     if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
         (vi8 && !aligned16(v_scales)) || (workspace && !aligned16(workspace)))
         return fail(FA_ERR_ALIGN, "fa_decode: q, k_cache, v_cache, v_scales, out and workspace "
                                   "must be 16-byte aligned");
-    if (!aligned_to(seq_lens, 4) || !aligned_to(block_table, 4) || !aligned_to(window, 4))
-        return fail(FA_ERR_ALIGN, "fa_decode: seq_lens, block_table and window must be 4-byte "
-                                  "aligned");
+    if (!aligned_to(seq_lens, 4) || !aligned_to(block_table, 4) || !aligned_to(window, 4) ||
+        !aligned_to(slot_ids, 4))
+        return fail(FA_ERR_ALIGN, "fa_decode: seq_lens, block_table, window and slot_ids must be "
+                                  "4-byte aligned");
     const int D = head_dim;
+    // a contiguous or ring cache holds one slot per sequence, or n_slots
+    // slots addressed through the slot map
+    const long long slots = slot_ids ? (long long)n_slots : (long long)batch;
     // aliasing: out against every input range we can size
     const size_t out_bytes = (size_t)batch * tq * n_q_heads * D * sizeof(float);
-    const size_t rows = paged ? (size_t)num_blocks * page_size : (size_t)batch * cap;
+    const size_t rows = paged ? (size_t)num_blocks * page_size : (size_t)slots * cap;
     const size_t kv_rows = rows * n_kv_heads;
     if (overlaps(out, out_bytes, q, (size_t)batch * tq * n_q_heads * D * 2) ||
         overlaps(out, out_bytes, k_cache, kv_rows * D * 2) ||
@@ -2672,7 +2778,8 @@ static int decode_impl(const void *q, const void *k_cache, const void *v_cache,
         (vi8 && overlaps(out, out_bytes, v_scales, kv_rows * (D / 32) * 2)) ||
         overlaps(out, out_bytes, seq_lens, (size_t)batch * 4) ||
         (paged && overlaps(out, out_bytes, block_table, (size_t)batch * max_blocks_per_seq * 4)) ||
-        (window && overlaps(out, out_bytes, window, (size_t)batch * 4)))
+        (window && overlaps(out, out_bytes, window, (size_t)batch * 4)) ||
+        (slot_ids && overlaps(out, out_bytes, slot_ids, (size_t)batch * 4)))
         return fail(FA_ERR_ALIAS, "fa_decode: out overlaps an input or the workspace");
     if (batch == 0)
         return 0;
@@ -2682,7 +2789,7 @@ static int decode_impl(const void *q, const void *k_cache, const void *v_cache,
         return rc;
     Path path = choose_path();
     const long long kv_rows_total = paged ? (long long)num_blocks * n_kv_heads * page_size
-                                          : (long long)batch * n_kv_heads * cap;
+                                          : slots * n_kv_heads * cap;
     if (kv_rows_total >= (1ll << 31)) {
         if (tq > 1 || chunk > 0)
             return fail(FA_ERR_LAYOUT, "fa_decode: caches of 2^31 rows or more are not "
@@ -2756,6 +2863,8 @@ static int decode_impl(const void *q, const void *k_cache, const void *v_cache,
     p.chunk = pl.chunk;
     p.max_chunks = pl.max_chunks;
     p.cpu = pl.cpu;
+    p.slot = slot_ids;
+    p.n_slots = static_cast<int>(slots);
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const dim3 grid = pl.path == Path::Mma ? dim3(pl.ctas)
@@ -2922,6 +3031,7 @@ FA_API int fa_append_kv(const float *k_new, const float *v_new, void *k_cache, v
     p.max_blocks = max_blocks_per_seq;
     p.num_blocks = num_blocks;
     p.cap = cap;
+    p.n_slots = batch;
     fa_append_kernel<<<batch * n_kv_heads, 128, 0, static_cast<cudaStream_t>(stream)>>>(
         p, k_new, v_new, static_cast<__half *>(k_cache), v_cache,
         static_cast<__half *>(v_scales), head_dim);
@@ -2931,35 +3041,41 @@ FA_API int fa_append_kv(const float *k_new, const float *v_new, void *k_cache, v
     return 0;
 }
 
-FA_API int fa_append_kv_ring(const float *k_new, const float *v_new, void *k_cache, void *v_cache,
-                             void *v_scales, const int32_t *positions, int batch, int n_kv_heads,
-                             int head_dim, int capacity, void *stream)
+// Append into contiguous per-slot rings or rows: fa_append_kv_ring (one slot
+// per sequence) and fa_append_kv_slots (slot map).
+static int append_contig(const char *name, const float *k_new, const float *v_new, void *k_cache,
+                         void *v_cache, void *v_scales, const int32_t *slot_ids,
+                         const int32_t *positions, int batch, int n_kv_heads, int head_dim,
+                         int n_slots, int capacity, bool ring, void *stream)
 {
     g_err[0] = 0;
     if (!k_new || !v_new || !k_cache || !v_cache || !positions)
-        return fail(FA_ERR_NULL, "fa_append_kv_ring: k_new, v_new, caches and positions are required");
+        return fail(FA_ERR_NULL, "%s: k_new, v_new, caches and positions are required", name);
     if (head_dim <= 0 || head_dim % 32)
-        return fail(FA_ERR_HEAD_DIM, "fa_append_kv_ring: head_dim %d must be a positive multiple of 32",
+        return fail(FA_ERR_HEAD_DIM, "%s: head_dim %d must be a positive multiple of 32", name,
                     head_dim);
     if (n_kv_heads <= 0)
-        return fail(FA_ERR_HEADS, "fa_append_kv_ring: n_kv_heads %d", n_kv_heads);
-    if (batch < 0 || capacity <= 0 || capacity % 16)
-        return fail(FA_ERR_LAYOUT, "fa_append_kv_ring: bad batch or capacity (a multiple of 16)");
+        return fail(FA_ERR_HEADS, "%s: n_kv_heads %d", name, n_kv_heads);
+    if (batch < 0 || capacity <= 0 || (ring && capacity % 16) || n_slots <= 0 ||
+        (double)n_slots * n_kv_heads * (double)capacity > 1e15)
+        return fail(FA_ERR_LAYOUT, "%s: bad batch, slot count or capacity (a multiple of 16 "
+                                   "for a ring)", name);
     const size_t new_bytes = (size_t)batch * n_kv_heads * head_dim * sizeof(float);
-    const size_t kv_rows = (size_t)batch * capacity * n_kv_heads;
-    const void *ins[3] = {k_new, v_new, positions};
-    const size_t in_bytes[3] = {new_bytes, new_bytes, (size_t)batch * 4};
-    for (int i = 0; i < 3; ++i)
+    const size_t kv_rows = (size_t)n_slots * capacity * n_kv_heads;
+    const void *ins[4] = {k_new, v_new, positions, slot_ids};
+    const size_t in_bytes[4] = {new_bytes, new_bytes, (size_t)batch * 4, (size_t)batch * 4};
+    for (int i = 0; i < 4; ++i)
         if (overlaps(k_cache, kv_rows * head_dim * 2, ins[i], in_bytes[i]) ||
             overlaps(v_cache, kv_rows * head_dim * (v_scales ? 1 : 2), ins[i], in_bytes[i]) ||
             (v_scales && overlaps(v_scales, kv_rows * (head_dim / 32) * 2, ins[i], in_bytes[i])))
-            return fail(FA_ERR_ALIAS, "fa_append_kv_ring: a cache overlaps k_new, v_new or positions");
+            return fail(FA_ERR_ALIAS, "%s: a cache overlaps k_new, v_new, positions or slot_ids",
+                        name);
     if (!aligned_to(k_new, 4) || !aligned_to(v_new, 4) || !aligned_to(positions, 4) ||
-        !aligned_to(k_cache, 2) || !aligned_to(v_cache, v_scales ? 1 : 2) ||
-        !aligned_to(v_scales, 2))
-        return fail(FA_ERR_ALIGN, "fa_append_kv_ring: a pointer is not aligned to its element type");
+        !aligned_to(slot_ids, 4) || !aligned_to(k_cache, 2) ||
+        !aligned_to(v_cache, v_scales ? 1 : 2) || !aligned_to(v_scales, 2))
+        return fail(FA_ERR_ALIGN, "%s: a pointer is not aligned to its element type", name);
     if ((long long)batch * n_kv_heads > 0x7fffffffll)
-        return fail(FA_ERR_LAYOUT, "fa_append_kv_ring: too many rows");
+        return fail(FA_ERR_LAYOUT, "%s: too many rows", name);
     if (batch == 0)
         return 0;
     Params p = {};
@@ -2970,14 +3086,39 @@ FA_API int fa_append_kv_ring(const float *k_new, const float *v_new, void *k_cac
     p.page_size = 16;
     p.max_blocks = capacity;
     p.cap = capacity;
-    p.ring = 1;
+    p.ring = ring ? 1 : 0;
+    p.slot = slot_ids;
+    p.n_slots = n_slots;
     fa_append_kernel<<<batch * n_kv_heads, 128, 0, static_cast<cudaStream_t>(stream)>>>(
         p, k_new, v_new, static_cast<__half *>(k_cache), v_cache,
         static_cast<__half *>(v_scales), head_dim);
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess)
-        return fail(FA_ERR_CUDA, "fa_append_kv_ring: launch failed: %s", cudaGetErrorString(e));
+        return fail(FA_ERR_CUDA, "%s: launch failed: %s", name, cudaGetErrorString(e));
     return 0;
+}
+
+FA_API int fa_append_kv_ring(const float *k_new, const float *v_new, void *k_cache, void *v_cache,
+                             void *v_scales, const int32_t *positions, int batch, int n_kv_heads,
+                             int head_dim, int capacity, void *stream)
+{
+    return append_contig("fa_append_kv_ring", k_new, v_new, k_cache, v_cache, v_scales, nullptr,
+                         positions, batch, n_kv_heads, head_dim, batch > 0 ? batch : 1, capacity,
+                         true, stream);
+}
+
+FA_API int fa_append_kv_slots(const float *k_new, const float *v_new, void *k_cache,
+                              void *v_cache, void *v_scales, const int32_t *slot_ids,
+                              const int32_t *positions, int batch, int n_kv_heads, int head_dim,
+                              int n_slots, int capacity, int ring, void *stream)
+{
+    if (!slot_ids) {
+        g_err[0] = 0;
+        return fail(FA_ERR_NULL, "fa_append_kv_slots: slot_ids is required");
+    }
+    return append_contig("fa_append_kv_slots", k_new, v_new, k_cache, v_cache, v_scales,
+                         slot_ids, positions, batch, n_kv_heads, head_dim, n_slots, capacity,
+                         ring != 0, stream);
 }
 
 FA_API int fa_gather_kv_debug(const void *cache, int row_bytes, const int32_t *block_table,

@@ -60,6 +60,7 @@ extern "C" {
 #define FA_STATUS_BAD_BLOCK 2u     /* a block-table entry was outside [0, num_blocks); tile skipped */
 #define FA_STATUS_WAIT_TIMEOUT 4u  /* a copy wait passed its ~1 s limit; that split's result is void */
 #define FA_STATUS_POS_RANGE 8u     /* fa_append_kv: a position outside [0, capacity); store skipped */
+#define FA_STATUS_BAD_SLOT 16u     /* a slot id outside [0, n_slots): zero row / store skipped */
 
 /*
  * fa_decode -- one decode step of attention for `batch` sequences.
@@ -231,6 +232,39 @@ FA_API int fa_decode_ring(const void *q, const void *k_cache, const void *v_cach
                           size_t workspace_bytes, void *stream);
 
 /*
+ * fa_decode_slots -- fa_decode over a pool of per-slot contiguous (ring = 0)
+ * or ring (ring = 1) caches, each batch row reading the slot a device-side
+ * slot map names.  The batched kernels of the mlx-native page
+ * (flash_attn_vec_hybrid_batched and its GQA / per-slot-bucket sibling) read
+ * per query row the row's slot (slot_id_arr) and position (seq_pos_arr) on
+ * the device and address that slot's [n_kv_heads][capacity][head_dim] rows;
+ * this is that indirection, so a server decodes only its active slots (any
+ * subset of the pool, in any order) without copying caches.
+ *
+ * k_cache, v_cache (and v_scales) [n_slots][n_kv_heads][capacity][...], the
+ *            contiguous layout of fa_decode (fa_decode_ring's when ring = 1).
+ * slot_ids   int32 [batch] (device): row b uses slot slot_ids[b].  A slot id
+ *            outside [0, n_slots) gives row b a zero output and sets
+ *            FA_STATUS_BAD_SLOT.  Rows may share a slot (read-only).
+ * q, out, seq_lens, window  per row, as fa_decode: seq_lens[b] is the length
+ *            of row b's slot (the page's seq_pos + 1; for a ring the tokens
+ *            the slot has seen, as fa_decode_ring).
+ * n_slots    slots in the pool; capacity  tokens per slot (a multiple of 16
+ *            for a ring or for int8 V).
+ * workspace  fa_decode_workspace_size(batch, n_q_heads, n_kv_heads, head_dim,
+ *            ring ? capacity + 16 : capacity, 0) bytes.
+ * Other arguments, rules and errors as fa_decode; slot_ids is 4-byte aligned
+ * (else FA_ERR_ALIGN).  The split plan covers the batch rows only, so idle
+ * slots cost nothing.
+ */
+FA_API int fa_decode_slots(const void *q, const void *k_cache, const void *v_cache,
+                           const void *v_scales, const int32_t *slot_ids,
+                           const int32_t *seq_lens, int n_q_heads, int n_kv_heads, int head_dim,
+                           float scale, const int32_t *window, void *out, int batch, int n_slots,
+                           int capacity, int ring, void *workspace, size_t workspace_bytes,
+                           void *stream);
+
+/*
  * fa_decode_workspace_size -- bytes of scratch fa_decode needs for these
  * sizes: the split-K partials (unnormalised O plus running max and sum per
  * query head and split; the "partial scratch B*H*chunks*(D+2)" of tessl's
@@ -291,6 +325,19 @@ FA_API int fa_append_kv_ring(const float *k_new, const float *v_new, void *k_cac
                              int head_dim, int capacity, void *stream);
 
 /*
+ * fa_append_kv_slots -- fa_append_kv (ring = 0) or fa_append_kv_ring
+ * (ring = 1) into the pool of fa_decode_slots: row b of k_new, v_new and
+ * positions writes slot slot_ids[b] (int32 [batch], device) at token
+ * positions[b].  A slot id outside [0, n_slots) stores nothing and sets
+ * FA_STATUS_BAD_SLOT.  Two rows naming the same slot and row race; give each
+ * row its own slot.  Other rules and errors as the append it extends.
+ */
+FA_API int fa_append_kv_slots(const float *k_new, const float *v_new, void *k_cache,
+                              void *v_cache, void *v_scales, const int32_t *slot_ids,
+                              const int32_t *positions, int batch, int n_kv_heads, int head_dim,
+                              int n_slots, int capacity, int ring, void *stream);
+
+/*
  * fa_gather_kv_debug -- copy sequence b's first n_tokens cache rows, through
  * the same page-address path fa_decode's loader uses, into dense
  * [n_kv_heads][n_tokens][row_bytes] (device).  row_bytes = 2*head_dim for K
@@ -342,9 +389,10 @@ FA_API int fa_decode_device_status(unsigned int *status, void *stream);
  *   - sizes whose scratch need (fa_decode_workspace_size) exceeds
  *     FA_NOALLOC_SCRATCH_BYTES are rejected with FA_ERR_WORKSPACE and a
  *     message stating both sizes; nothing is launched;
- *   - the first call on a device looks up the array's device address on that
- *     device (once per device, with it current); make that first call before
- *     any stream capture begins;
+ *   - the first call in a CUDA context (for runtime-API callers: the first
+ *     call on a device) looks up the array's device address in that context,
+ *     with it current, and caches it under the context's id; make that
+ *     first call before any stream capture begins;
  *   - all calls share the one array: calls whose kernels overlap on the GPU
  *     (different streams, or different host threads on one device) race on
  *     it and give wrong results.  Serialise them, e.g. on one stream.  The

@@ -242,3 +242,34 @@ except RuntimeError as e:
                        timeout=300)
     assert r.returncode == 0, r.stderr
     assert "absent: raised" in r.stdout and "build: nvcc failed" in r.stdout, r.stdout
+
+
+def test_slots_reject_bad_arguments(lib):
+    f = lib.fa_decode_slots
+    #             q  k      v      vs    slots  sl     hq hkv d    scale win  out    B  n   cap  ring
+    def args(**kw):
+        a = dict(q=A, k=2 * A, v=3 * A, vs=None, si=7 * A, sl=4 * A, out=5 * A, ns=64, cap=512,
+                 ring=0)
+        a.update(kw)
+        return (a["q"], a["k"], a["v"], a["vs"], a["si"], a["sl"], 8, 2, 128, 0.1, None,
+                a["out"], 1, a["ns"], a["cap"], a["ring"], 6 * A, 1 << 30, None)
+    assert f(*args(si=None)) == -1
+    assert f(*args(ns=0)) == -6
+    assert f(*args(cap=0)) == -6
+    assert f(*args(ring=1, cap=100)) == -6               # a ring's capacity: a multiple of 16
+    assert f(*args(vs=8 * A, cap=100)) == -6             # contiguous int8 V likewise
+    assert f(*args(si=7 * A + 2)) == -9                  # slot_ids: 4-byte aligned
+    assert f(*args(out=7 * A)) == -7                     # out over the slot map
+    g = lib.fa_append_kv_slots
+    #               k_new v_new k_cache v_cache sc  slots pos  B  Hkv D   n   cap ring
+    def gargs(**kw):
+        a = dict(si=7 * A, pos=4 * A, ns=8, cap=64, ring=0, kn=A)
+        a.update(kw)
+        return (a["kn"], A + 4096, 2 * A, 3 * A, None, a["si"], a["pos"], 1, 2, 128, a["ns"],
+                a["cap"], a["ring"], None)
+    assert g(*gargs(si=None)) == -1
+    assert g(*gargs(ns=0)) == -6
+    assert g(*gargs(ring=1, cap=40)) == -6
+    assert g(*gargs(si=7 * A + 1)) == -9
+    # the K pool (8 slots x 2 x 64 x 128 fp16 = 256 KiB from 2A) would hold the slot map
+    assert g(*gargs(si=2 * A + 65536)) == -7

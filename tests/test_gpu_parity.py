@@ -61,7 +61,8 @@ SMALL = [
 
 @pytest.fixture(params=["mma", "simt"])
 def kernel(request, monkeypatch):
-    """Run a case through each split kernel (int8 V always takes the CUDA-core one)."""
+    """Run a case through each split kernel: the tensor-core stream-K one and the
+    CUDA-core one (FA_DECODE_KERNEL=simt), int8 V cases included."""
     monkeypatch.setenv("FA_DECODE_KERNEL", request.param)
     return request.param
 

@@ -14,7 +14,7 @@ import torch
 from decode_step_kv_gb300 import binding
 from decode_step_kv_gb300.inputs import Workload
 
-from _helpers import assert_close, build_case, gpu_decode, to_cuda
+from _helpers import assert_close, build_case, gpu_decode, oracle_decode, to_cuda
 
 pytestmark = pytest.mark.gpu
 
@@ -33,22 +33,27 @@ def _noalloc(wl, d):
     return out
 
 
+@pytest.mark.parametrize("paged", [True, False])
 @pytest.mark.parametrize("v_int8", [False, True])
-def test_noalloc_matches_fa_decode_on_two_calls_in_a_row(v_int8):
-    wl = Workload("noalloc", 4, 16, 4, 128, paged=True, v_int8=v_int8, window=1000,
-                  window_odd_only=True, seed=4242)
+def test_noalloc_matches_fa_decode_on_two_calls_in_a_row(v_int8, paged):
+    """Two calls in a row through the C ABI, each compared with fa_decode on
+    the same inputs and, independently of both, with the fp64 oracle; paged
+    and contiguous caches (the contiguous capacity a multiple of 16)."""
+    wl = Workload("noalloc", 4, 16, 4, 128, paged=paged, v_int8=v_int8, window=1000,
+                  window_odd_only=True, seed=4242 + 2 * paged + v_int8)
     # the first call uses long sequences (many splits), the second short and
     # ragged ones, so the second reads only scratch it wrote itself
     for lens in ([9000, 12000, 7000, 16000], [300, 17, 5000, 1]):
         inp = build_case(wl, seq_lens=lens, capacity=16000)
         d = to_cuda(inp)
-        cap = d["max_blocks"] * wl.page_size
+        cap = d["max_blocks"] * (wl.page_size if paged else 1)
         assert binding.fa_decode_workspace_size(4, 16, 4, 128, cap) > 0   # scratch is used
         want = gpu_decode(wl, d).cpu().numpy()
         got = _noalloc(wl, d)
         torch.cuda.synchronize()
         got = got.cpu().numpy()
-        assert_close(got, want, v_int8, f"noalloc lens={lens}")
+        assert_close(got, want, v_int8, f"noalloc vs fa_decode lens={lens}")
+        assert_close(got, oracle_decode(wl, inp), v_int8, f"noalloc vs oracle lens={lens}")
 
 
 def test_noalloc_rejects_sizes_beyond_its_scratch():
