@@ -369,7 +369,7 @@ def time_steps(step, nbytes, steps, warmup, device):
 def time_next_rows(steps, device, peak):
     """The rows beyond the plain decode step, each timed under the headline's
     protocol on seeded inputs of the decode shapes: ring-cache decode,
-    multi-query decode, cache append."""
+    slot-map decode, multi-query decode, cache append."""
     import torch
     from decode_step_kv_gb300 import binding
     from decode_step_kv_gb300.inputs import WORKLOADS, kv_bytes, make_inputs, make_queries
@@ -395,6 +395,47 @@ def time_next_rows(steps, device, peak):
                    "us_per_step": round(us, 2), "kv_bytes": nbytes, "GB/s": round(gbs, 1),
                    "frac_of_peak": round(gbs / peak, 4)}
     del d, ws, out
+    torch.cuda.empty_cache()
+
+    # slot map: 8 active slots of a pool of 64 contiguous per-slot caches (32
+    # q / 8 kv heads, D=128, 16K keys per slot) through fa_decode_slots, and
+    # the same 8 rows decoded the way a caller without the map must: a
+    # 64-row fa_decode whose 56 idle rows have length 0
+    n_slots, C = 64, 16384
+    wl = dataclasses.replace(WORKLOADS["32x32k_d128_paged"], name="slots", batch=n_slots,
+                             paged=False, seq_lens=(C,) * n_slots)
+    d = make_inputs(wl, device, capacity=C)
+    B, Hq, Hkv, D = 8, wl.n_q_heads, wl.n_kv_heads, wl.head_dim
+    g = torch.Generator(device="cpu").manual_seed(wl.seed + 3000)
+    active = torch.randperm(n_slots, generator=g)[:B].to(torch.int32)
+    slot_ids = active.to(device)
+    lens = torch.full((B,), C, dtype=torch.int32, device=device)
+    q8 = d["q"][:B].contiguous()
+    nbytes = B * C * Hkv * D * 4
+    ws = binding.alloc_workspace(B, Hq, Hkv, D, C, device=device)
+    out = torch.empty((B, Hq, D), dtype=torch.float32, device=device)
+    us = time_steps(lambda: binding.fa_decode_slots(
+        q8, d["k_cache"], d["v_cache"], None, slot_ids, lens, Hq, Hkv, D, wl.scale, None, out,
+        workspace=ws, stream=stream), nbytes, steps, 3, device)
+    q64 = torch.zeros_like(d["q"])
+    q64[active.long()] = q8
+    lens64 = torch.zeros((n_slots,), dtype=torch.int32)
+    lens64[active.long()] = C
+    lens64 = lens64.to(device)
+    ws64 = binding.alloc_workspace(n_slots, Hq, Hkv, D, C, device=device)
+    out64 = torch.empty((n_slots, Hq, D), dtype=torch.float32, device=device)
+    us64 = time_steps(lambda: binding.fa_decode(
+        q64, d["k_cache"], d["v_cache"], None, None, lens64, Hq, Hkv, D, wl.scale, None, out64,
+        batch=n_slots, max_blocks_per_seq=C, workspace=ws64, stream=stream), nbytes, steps, 3,
+        device)
+    gbs = nbytes / (us * 1e-6) / 1e9
+    res["slots_8_of_64"] = {
+        "workload": "8 active slots (seeded permutation) of a 64-slot pool of contiguous caches, "
+                    "32 q/8 kv heads, D=128, 16384 keys per active slot",
+        "us_per_step": round(us, 2), "kv_bytes": nbytes, "GB/s": round(gbs, 1),
+        "frac_of_peak": round(gbs / peak, 4),
+        "all_64_rows_idle_len0_us_per_step": round(us64, 2)}
+    del d, ws, ws64, out, out64, q64
     torch.cuda.empty_cache()
 
     # multi-query decode (speculative verify) on 32x32k_d128_paged's shape: with G = 4,

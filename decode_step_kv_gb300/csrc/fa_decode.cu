@@ -824,24 +824,50 @@ __device__ __forceinline__ long long tile_row(const Params &p, int b, int kv, in
 // Per-sequence walk over the flattened tile space.  Units (one KV head and
 // head group of one sequence) are ordered by (sequence, unit); the tiles of
 // a unit are its 16-token tiles intersecting the attended range [lo, hi).
+//
+// The stream-K plan charges each unit's start UNIT_COST tiles of work (the
+// query load and the partial write a worker pays on entering a new unit):
+// a unit takes n + UNIT_COST positions of the flattened space that workers
+// split evenly, UNIT_COST empty ones then its n tiles, so a worker whose
+// range crosses into a new unit gets that many fewer tiles.  Position of
+// tile k of unit j of sequence b: P_b + j*(n_b + c) + c + k, with c =
+// UNIT_COST (stream-K plan) or 0 (batch-invariant plan, which cuts real
+// tiles).
+#ifndef FA_UNIT_COST
+#define FA_UNIT_COST 2
+#endif
+constexpr int UNIT_COST = FA_UNIT_COST;
+
+// Flattened positions sequence b takes in the stream-K plan: its units x
+// (n + UNIT_COST), none when it has no tiles.
+__device__ __forceinline__ long long seq_span(const Params &p, int n)
+{
+    return n > 0 ? (long long)(n + UNIT_COST) * p.U_b : 0;
+}
+
 struct Walk {
     int b, j, k, n, lo, hi;   // sequence, unit in sequence, tile in unit, tiles per unit
-    long long P;              // flattened index of sequence b's first tile
+    int c;                    // empty positions before each unit's tiles
+    long long P;              // flattened position of sequence b's first unit
 
     __device__ __forceinline__ void load(const Params &p)
     {
         attended_range(p, b, lo, hi, false);
         n = tiles_in<TILE>(lo, hi);
     }
-    // position at flattened tile t of sequence b_ (whose first tile is P_)
-    __device__ __forceinline__ void init(const Params &p, int b_, long long P_, long long t)
+    // position at the first tile at or after flattened position t of
+    // sequence b_ (whose first unit starts at P_)
+    __device__ __forceinline__ void init(const Params &p, int b_, long long P_, long long t,
+                                         int c_)
     {
         b = b_;
         P = P_;
+        c = c_;
         load(p);
         const long long off = t - P;
-        j = static_cast<int>(off / n);
-        k = static_cast<int>(off % n);
+        j = static_cast<int>(off / (n + c));
+        const int r = static_cast<int>(off % (n + c));
+        k = r < c ? 0 : r - c;
     }
     __device__ __forceinline__ void next(const Params &p)
     {
@@ -852,7 +878,8 @@ struct Walk {
             return;
         j = 0;
         do {
-            P += (long long)p.U_b * n;
+            if (n > 0)
+                P += (long long)p.U_b * (n + c);
             ++b;
             if (b >= p.B)
                 return;
@@ -864,12 +891,24 @@ struct Walk {
     {
         return (long long)b * p.U_b + j;
     }
-    __device__ __forceinline__ long long unit_start() const { return P + (long long)j * n; }
+    // flattened position of the unit's first tile, and of the current tile
+    __device__ __forceinline__ long long unit_start() const
+    {
+        return P + (long long)j * (n + c) + c;
+    }
+    __device__ __forceinline__ long long pos() const { return unit_start() + k; }
+    // whether the next tile (the following unit's first at a unit's end) lies
+    // at or beyond flattened position t1
+    __device__ __forceinline__ bool last_before(long long t1) const
+    {
+        return pos() + 1 + (k == n - 1 ? c : 0) >= t1;
+    }
 };
 
-// Warp-cooperative scan over the sequences: T = all tiles of the step; when
-// target >= 0 also the sequence holding flattened tile `target` and that
-// sequence's first flattened tile.  Every lane returns the same values.
+// Warp-cooperative scan over the sequences: T = the flattened positions of
+// the step (tiles plus UNIT_COST per unit); when target >= 0 also the
+// sequence holding position `target` and that sequence's first position.
+// Every lane returns the same values.
 __device__ __forceinline__ long long flat_scan(const Params &p, long long target, int &b_at,
                                                long long &P_at, bool report = false,
                                                long long *pref = nullptr)
@@ -884,7 +923,7 @@ __device__ __forceinline__ long long flat_scan(const Params &p, long long target
         if (b < p.B) {
             int lo, hi;
             attended_range(p, b, lo, hi, report);
-            c = (long long)tiles_in<TILE>(lo, hi) * p.U_b;
+            c = seq_span(p, tiles_in<TILE>(lo, hi));
         }
         long long x = c;
 #pragma unroll
@@ -1070,7 +1109,6 @@ __global__ void __launch_bounds__(Cfg<D, VI8>::NW * 32, 1)
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmV))
                          : "memory");
     }
-
     int b_at = -1;
     long long P_at = 0;
     long long T, t0, t1;
@@ -1113,7 +1151,7 @@ __global__ void __launch_bounds__(Cfg<D, VI8>::NW * 32, 1)
             if (b < p.B) {
                 int lo, hi;
                 attended_range(p, b, lo, hi, w == 0);   // worker 0 reports clamped lengths
-                c[i] = (long long)tiles_in<TILE>(lo, hi) * p.U_b;
+                c[i] = seq_span(p, tiles_in<TILE>(lo, hi));
             }
             x[i] = c[i];
 #pragma unroll
@@ -1157,7 +1195,8 @@ __global__ void __launch_bounds__(Cfg<D, VI8>::NW * 32, 1)
         t1 = range_start(w + 1, T, We);
         flat_scan(p, t0, b_at, P_at);
     }
-    const int n_my = static_cast<int>(t1 - t0);
+    // [t0, t1): this worker's flattened positions; its tiles are the ones in
+    // there (the stream-K plan's unit-start positions hold none)
 
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem = reinterpret_cast<unsigned char *>(
@@ -1178,7 +1217,7 @@ __global__ void __launch_bounds__(Cfg<D, VI8>::NW * 32, 1)
 
     const uint64_t policy = evict_first_policy();
     Walk pw;                          // producer position (lane 0 issues)
-    pw.init(p, b_at, P_at, t0);
+    pw.init(p, b_at, P_at, t0, BI ? 0 : UNIT_COST);
     Walk cw = pw;                     // consumer position
 
     auto issue = [&](int s) {
@@ -1206,14 +1245,6 @@ __global__ void __launch_bounds__(Cfg<D, VI8>::NW * 32, 1)
                      policy);
         }
     };
-
-    const int n_pre = n_my < STAGES ? n_my : STAGES;
-    for (int s = 0; s < n_pre; ++s) {
-        if (lane == 0)
-            issue(s);
-        pw.next(p);
-    }
-    __syncwarp();
 
     // Q^T of the current unit as the QK B operand, per column group gi:
     // b0 = q[column gi*8 + g4][16ks+2t4..], b1 = +8; plus this lane's two
@@ -1267,6 +1298,33 @@ __global__ void __launch_bounds__(Cfg<D, VI8>::NW * 32, 1)
             column_range(p, u.b, u.hi, c1.live ? c1.j : tq - 1, clo[gi][1], chi[gi][1]);
         }
     };
+    // Whether a tile remains to be issued: at head_dim 128 the producer's
+    // position is checked against t1; at head_dim 256 the worker's tiles are
+    // counted once up front (a walk over the units in its range) and the
+    // loop runs on the count.  Both give the same tiles; each form measured
+    // faster for its head_dim (the 256 kernels run at the register limit).
+    constexpr bool POS_LOOP = D == 128;
+    int n_my = 0;
+    if constexpr (!POS_LOOP) {
+        Walk e = pw;
+        while (e.pos() < t1) {
+            const long long us = e.unit_start();
+            const long long end = us + e.n < t1 ? us + e.n : t1;
+            n_my += static_cast<int>(end - e.pos());
+            if (us + e.n >= t1)
+                break;
+            e.k = e.n - 1;          // on to the next unit
+            e.next(p);
+        }
+    }
+    int n_iss = 0;                    // tiles issued so far (tile i lands in stage i % STAGES)
+    while (n_iss < STAGES && (POS_LOOP ? pw.pos() < t1 : n_iss < n_my)) {
+        if (lane == 0)
+            issue(n_iss);
+        pw.next(p);
+        ++n_iss;
+    }
+    __syncwarp();
     load_q(cw);
     // pull a unit's query rows into L2 when its first tile is issued, so the
     // switch to that unit does not wait on HBM (lane: column lane/4, line lane%4)
@@ -1297,7 +1355,7 @@ __global__ void __launch_bounds__(Cfg<D, VI8>::NW * 32, 1)
 
     int i_fail = -1;
     int ck = 0;     // batch-invariant plan: tile within the chunk (ranges start on a chunk)
-    for (int i = 0; i < n_my; ++i) {
+    for (int i = 0; i < (POS_LOOP ? n_iss : n_my); ++i) {
         const int s = i % STAGES;
         if (!mbar_wait_warp(my_bars + 8 * s, (i / STAGES) & 1)) {
             if (lane == 0)
@@ -1489,16 +1547,18 @@ __global__ void __launch_bounds__(Cfg<D, VI8>::NW * 32, 1)
         if constexpr (VI8 && FA_I8_INPLACE)
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // before TMA refills it
         __syncwarp();
-        if (i + STAGES < n_my) {
+        if (POS_LOOP ? pw.pos() < t1 : i + STAGES < n_my) {   // tile i + STAGES refills stage s
             if (pw.k == 0)
                 prefetch_q(pw);
             if (lane == 0)
                 issue(s);
             pw.next(p);
+            if constexpr (POS_LOOP)
+                ++n_iss;
         }
         __syncwarp();
 
-        if (cw.k == cw.n - 1 || i == n_my - 1 ||
+        if (cw.k == cw.n - 1 || i + 1 == (POS_LOOP ? n_iss : n_my) ||
             (BI && ck == p.chunk - 1)) {
             // ---- end of this worker's segment of the unit (with the
             // batch-invariant plan: of a chunk): publish it
@@ -1567,7 +1627,7 @@ __global__ void __launch_bounds__(Cfg<D, VI8>::NW * 32, 1)
                 }
             }
             reset();
-            if (i + 1 < n_my) {
+            if (i + 1 < (POS_LOOP ? n_iss : n_my)) {
                 cw.next(p);
                 if (!BI || cw.k == 0)    // a new unit (not just the next chunk)
                     load_q(cw);
@@ -1579,7 +1639,7 @@ __global__ void __launch_bounds__(Cfg<D, VI8>::NW * 32, 1)
         }
     }
     if (i_fail >= 0)
-        for (int ii = i_fail; ii < n_my && ii < i_fail + STAGES; ++ii)
+        for (int ii = i_fail; ii < (POS_LOOP ? n_iss : n_my) && ii < i_fail + STAGES; ++ii)
             mbar_wait_warp(my_bars + 8 * (ii % STAGES), (ii / STAGES) & 1);
 }
 
@@ -1662,7 +1722,7 @@ __global__ void __launch_bounds__(MERGE_THREADS) fa_stream_merge_kernel(const Pa
                 if (bb < b) {
                     int l2, h2;
                     attended_range(p, bb, l2, h2, false);
-                    c = (long long)tiles_in<TILE>(l2, h2) * p.U_b;
+                    c = seq_span(p, tiles_in<TILE>(l2, h2));
                 }
 #pragma unroll
                 for (int off = 16; off >= 1; off >>= 1)
@@ -1684,7 +1744,7 @@ __global__ void __launch_bounds__(MERGE_THREADS) fa_stream_merge_kernel(const Pa
         __syncthreads();
         const long long T = sh_T;
         const int We = workers_for(p, T);
-        const long long us = sh_P + (long long)j * n;
+        const long long us = sh_P + (long long)j * (n + UNIT_COST) + UNIT_COST;   // first tile
         const int wf = worker_of(us, T, We);
         const int wl = worker_of(us + n - 1, T, We);
         if (wf == wl)
@@ -1851,7 +1911,7 @@ __global__ void __launch_bounds__(MERGE_ROWS_PER_CTA * 32) fa_stream_merge_rows_
             if (bb < b) {
                 int l2, h2;
                 attended_range(p, bb, l2, h2, false);
-                c = (long long)tiles_in<TILE>(l2, h2) * p.U_b;
+                c = seq_span(p, tiles_in<TILE>(l2, h2));
             }
 #pragma unroll
             for (int off = 16; off >= 1; off >>= 1)
@@ -1864,7 +1924,7 @@ __global__ void __launch_bounds__(MERGE_ROWS_PER_CTA * 32) fa_stream_merge_rows_
         P = p.pref[b];
     }
     const int We = workers_for(p, T);
-    const long long us = P + (long long)j * n;
+    const long long us = P + (long long)j * (n + UNIT_COST) + UNIT_COST;   // first tile
     const int wf = worker_of(us, T, We);
     const int wl = worker_of(us + n - 1, T, We);
     if (wf == wl)
@@ -2197,11 +2257,14 @@ static Plan make_plan(Path path, int B, int Hq, int Hkv, int D, long long cap, i
         }
         pl.ctas = (num_sms > 0 ? num_sms : 1) * cps;
         if (chunk == 0 && FA_GRID_CAP) {
-            // no more workers than the capacity can give MIN_TPW tiles each: a
-            // step's tiles are at most batch x units x ceil(capacity / 16),
+            // no more workers than the capacity can give MIN_TPW positions
+            // each: a step's tiles are at most batch x units x ceil(capacity / 16),
             // so a small step launches only the CTAs it can use (the device
             // plan still sizes itself from the real lengths)
-            const long long max_t = (long long)B * pl.units * ((cap + tc::TILE - 1) / tc::TILE);
+            // (positions: tiles plus the unit-start cost the device plan
+            // charges, so a small step still gets a worker per tile)
+            const long long max_t = (long long)B * pl.units *
+                                    ((cap + tc::TILE - 1) / tc::TILE + tc::UNIT_COST);
             const long long w_cap = (max_t + tc::MIN_TPW - 1) / tc::MIN_TPW;
             const long long c_cap = (w_cap + nw - 1) / nw;
             if (c_cap < pl.ctas)
