@@ -808,6 +808,38 @@ __device__ __forceinline__ uint32_t swz(uint32_t base, int row, int chunk)
     return base + box * (TILE * 128) + row * 128 + c * 16;
 }
 
+// Distributed shared memory: the address of shared location `local` (an
+// address in this CTA's window) in cluster CTA `rank`, and loads from it.
+__device__ __forceinline__ uint32_t cl_map(uint32_t local, uint32_t rank)
+{
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ float2 cl_ld2(uint32_t a)
+{
+    float2 v;
+    asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(a)
+                 : "memory");
+    return v;
+}
+__device__ __forceinline__ float4 cl_ld4(uint32_t a)
+{
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(a)
+                 : "memory");
+    return v;
+}
+// Every thread of every CTA of the cluster: writes before the barrier are
+// visible to the cluster's reads after it.
+__device__ __forceinline__ void cluster_sync()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 // Tile row coordinate (the tensor maps view K and V as [rows][D]); -1 for a
 // block id out of range.
 __device__ __forceinline__ long long tile_row(const Params &p, int b, int kv, int tok)
@@ -1085,8 +1117,12 @@ __device__ __forceinline__ void column_range(const Params &p, int b, int L, int 
 // instantiation, so the default kernel carries none of its code).  NG: column
 // groups of 8 (query, head) columns a warp carries per K/V tile; 2 lets a
 // unit hold 16 columns, so more than 8 columns per KV head read each tile
-// once instead of once per group.
-template <int D, bool VI8, bool BI, int NG>
+// once instead of once per group.  CL: the cluster plan for small steps --
+// one thread-block cluster of CL_CTAS CTAs per unit, the unit's tiles split
+// evenly over the cluster's warps, and the warps' partials folded through
+// distributed shared memory at the end, so no merge kernel runs.
+constexpr int CL_CTAS = 8;      // CTAs per cluster (the portable maximum)
+template <int D, bool VI8, bool BI, int NG, bool CL = false>
 __global__ void __launch_bounds__(Cfg<D, VI8>::NW * 32, 1)
     fa_stream_mma_kernel(const Params p, const __grid_constant__ CUtensorMap tmK,
                          const __grid_constant__ CUtensorMap tmV)
@@ -1111,9 +1147,25 @@ __global__ void __launch_bounds__(Cfg<D, VI8>::NW * 32, 1)
     }
     int b_at = -1;
     long long P_at = 0;
-    long long T, t0, t1;
-    int We;
-    if constexpr (BI) {
+    long long T = 0, t0 = 0, t1 = 0;
+    int We = 0;
+    int cl_j = 0, cl_n = 0;           // cluster plan: the cluster's unit and its tiles
+    if constexpr (CL) {
+        // cluster plan: unit u = cluster index; worker r of the cluster's
+        // CL_CTAS x NW warps takes tiles [r*n/R, (r+1)*n/R) of it.  No warp
+        // leaves early: every thread must reach the cluster barriers below.
+        const int u = blockIdx.x / CL_CTAS;
+        b_at = u / p.U_b;
+        cl_j = u % p.U_b;
+        int lo, hi;
+        attended_range(p, b_at, lo, hi, blockIdx.x % CL_CTAS == 0 && threadIdx.x == 0);
+        cl_n = tiles_in<TILE>(lo, hi);
+        constexpr int R = CL_CTAS * C::NW;
+        const int r = (blockIdx.x % CL_CTAS) * C::NW + warp;
+        t0 = (long long)r * cl_n / R;
+        t1 = (long long)(r + 1) * cl_n / R;
+        P_at = -(long long)cl_j * cl_n;   // positions count from the unit's first tile
+    } else if constexpr (BI) {
         // batch-invariant plan: whole chunks per worker; [t0, t1) is the
         // tile range of chunks [c0, c1)
         long long Pc;
@@ -1217,7 +1269,15 @@ __global__ void __launch_bounds__(Cfg<D, VI8>::NW * 32, 1)
 
     const uint64_t policy = evict_first_policy();
     Walk pw;                          // producer position (lane 0 issues)
-    pw.init(p, b_at, P_at, t0, BI ? 0 : UNIT_COST);
+    if (!CL || t1 > t0)
+        pw.init(p, b_at, P_at, t0, (BI || CL) ? 0 : UNIT_COST);
+    else {
+        pw.b = b_at;                  // a cluster-plan warp without tiles
+        pw.j = cl_j;
+        pw.k = pw.n = pw.c = 0;
+        pw.lo = pw.hi = 0;
+        pw.P = 0;
+    }
     Walk cw = pw;                     // consumer position
 
     auto issue = [&](int s) {
@@ -1303,9 +1363,11 @@ __global__ void __launch_bounds__(Cfg<D, VI8>::NW * 32, 1)
     // counted once up front (a walk over the units in its range) and the
     // loop runs on the count.  Both give the same tiles; each form measured
     // faster for its head_dim (the 256 kernels run at the register limit).
-    constexpr bool POS_LOOP = D == 128;
+    constexpr bool POS_LOOP = D == 128 && !CL;
     int n_my = 0;
-    if constexpr (!POS_LOOP) {
+    if constexpr (CL) {
+        n_my = static_cast<int>(t1 - t0);
+    } else if constexpr (!POS_LOOP) {
         Walk e = pw;
         while (e.pos() < t1) {
             const long long us = e.unit_start();
@@ -1569,6 +1631,26 @@ __global__ void __launch_bounds__(Cfg<D, VI8>::NW * 32, 1)
                     l[gi][0] += __shfl_xor_sync(0xffffffffu, l[gi][0], mask);
                     l[gi][1] += __shfl_xor_sync(0xffffffffu, l[gi][1], mask);
                 }
+            if constexpr (CL) {
+                // cluster plan: the warp's partial waits in its drained ring,
+                // [column][D] floats then [column] (m, l), for the fold below
+                float *part = reinterpret_cast<float *>(smem + warp * C::WARP_BYTES);
+                float2 *pml = reinterpret_cast<float2 *>(part + CPU * D);
+                const int h0 = 2 * t4, h1 = h0 + 1;
+#pragma unroll
+                for (int mt = 0; mt < KS; ++mt) {
+                    const int d = mt * 16 + g4;
+                    part[h0 * D + d] = acc[0][mt][0];
+                    part[h0 * D + d + 8] = acc[0][mt][2];
+                    part[h1 * D + d] = acc[0][mt][1];
+                    part[h1 * D + d + 8] = acc[0][mt][3];
+                }
+                if (g4 == 0) {
+                    pml[h0] = make_float2(m[0][0], l[0][0]);
+                    pml[h1] = make_float2(m[0][1], l[0][1]);
+                }
+                continue;        // the warp's last tile: its range lies in one unit
+            }
             bool whole;          // the segment is the whole unit: normalised output
             long long slot;      // else its partial's workspace slot
             if constexpr (BI) {
@@ -1641,6 +1723,104 @@ __global__ void __launch_bounds__(Cfg<D, VI8>::NW * 32, 1)
     if (i_fail >= 0)
         for (int ii = i_fail; ii < (POS_LOOP ? n_iss : n_my) && ii < i_fail + STAGES; ++ii)
             mbar_wait_warp(my_bars + 8 * (ii % STAGES), (ii / STAGES) & 1);
+
+    if constexpr (CL) {
+        // ---- cluster plan: fold the unit's partials through distributed
+        // shared memory.  A warp without tiles (or whose copies timed out)
+        // leaves an empty partial: max -inf, sum 0.
+        const uint32_t base = smem_u32(smem);
+        if (n_my == 0 || i_fail >= 0) {
+            // zero O as well, so the fold weighs every partial without a branch
+            float4 *po = reinterpret_cast<float4 *>(smem + warp * C::WARP_BYTES);
+            for (int x = lane; x < CPU * D / 4; x += 32)
+                po[x] = make_float4(0.f, 0.f, 0.f, 0.f);
+            float2 *pml = reinterpret_cast<float2 *>(po + CPU * D / 4);
+            if (lane < CPU)
+                pml[lane] = make_float2(-INFINITY, 0.f);
+        }
+        __syncwarp();
+        cluster_sync();
+        uint32_t rank;
+        asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(rank));
+        // column c of the unit: warp c / CL_CTAS of cluster CTA c % CL_CTAS
+        const int c = warp * CL_CTAS + static_cast<int>(rank);
+        if (c < nh) {
+            constexpr int R = CL_CTAS * C::NW;          // partials: one per warp of the cluster
+            static_assert(R % 8 == 0, "partials come in batches of 8");
+            constexpr int PPL = (R + 31) / 32;          // partials per lane
+            constexpr int EPL2 = D / 32;                // output floats per lane
+            float wv[PPL], Lsum = 0.f, M = -INFINITY;
+            float mv[PPL], lv[PPL];
+#pragma unroll
+            for (int q = 0; q < PPL; ++q) {
+                const int i = lane + 32 * q;
+                mv[q] = -INFINITY;
+                lv[q] = 0.f;
+                if (i < R) {
+                    const float2 x = cl_ld2(cl_map(base + (i % C::NW) * C::WARP_BYTES +
+                                                       (CPU * D + 2 * c) * 4,
+                                                   i / C::NW));
+                    mv[q] = x.x;
+                    lv[q] = x.y;
+                }
+                M = fmaxf(M, mv[q]);
+            }
+#pragma unroll
+            for (int off = 16; off >= 1; off >>= 1)
+                M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+#pragma unroll
+            for (int q = 0; q < PPL; ++q) {
+                wv[q] = mv[q] == -INFINITY ? 0.f : ex2(mv[q] - M);
+                Lsum = fmaf(lv[q], wv[q], Lsum);
+            }
+#pragma unroll
+            for (int off = 16; off >= 1; off >>= 1)
+                Lsum += __shfl_xor_sync(0xffffffffu, Lsum, off);
+            float o[EPL2];
+#pragma unroll
+            for (int e = 0; e < EPL2; ++e)
+                o[e] = 0.f;
+            // eight partials' loads in flight before their sums (empty
+            // partials hold zeros and weigh 0)
+            constexpr int BATCH = 8;
+            for (int i0 = 0; i0 < R; i0 += BATCH) {
+                float4 x[BATCH][EPL2 / 4];
+#pragma unroll
+                for (int u = 0; u < BATCH; ++u) {
+                    const int i = i0 + u;
+                    const uint32_t src = cl_map(base + (i % C::NW) * C::WARP_BYTES +
+                                                    (c * D + lane * EPL2) * 4,
+                                                i / C::NW);
+#pragma unroll
+                    for (int e = 0; e < EPL2 / 4; ++e)
+                        x[u][e] = cl_ld4(src + e * 16);
+                }
+#pragma unroll
+                for (int u = 0; u < BATCH; ++u) {
+                    const int i = i0 + u;
+                    const float a = __shfl_sync(0xffffffffu, wv[i / 32], i % 32);
+#pragma unroll
+                    for (int e = 0; e < EPL2 / 4; ++e) {
+                        o[4 * e] = fmaf(x[u][e].x, a, o[4 * e]);
+                        o[4 * e + 1] = fmaf(x[u][e].y, a, o[4 * e + 1]);
+                        o[4 * e + 2] = fmaf(x[u][e].z, a, o[4 * e + 2]);
+                        o[4 * e + 3] = fmaf(x[u][e].w, a, o[4 * e + 3]);
+                    }
+                }
+            }
+            const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
+            const Col cq = column(p, cl_j / p.n_hg, cl_j % p.n_hg, c, CPU);
+            float4 *dst = reinterpret_cast<float4 *>(
+                p.out + (((long long)b_at * tq + cq.j) * p.Hq + cq.h) * D + lane * EPL2);
+#pragma unroll
+            for (int e = 0; e < EPL2; e += 4)
+                dst[e / 4] = make_float4(o[e] * inv, o[e + 1] * inv, o[e + 2] * inv,
+                                         o[e + 3] * inv);
+        }
+        // no CTA leaves while another may still read its shared memory
+        __syncwarp();
+        cluster_sync();
+    }
 }
 
 // Log-sum-exp merge for the stream-K kernel: one CTA of MERGE_THREADS per
@@ -2470,6 +2650,80 @@ static cudaError_t launch_mma(const Params &p, const CUtensorMap &tmK, const CUt
     return cudaGetLastError();
 }
 
+// Cluster plan (tc::CL_CTAS CTAs per unit, no merge kernel): the largest
+// unit it takes, in 16-token tiles, beyond which the stream-K plan's use of
+// every SM wins over saving the merge kernel.  Measured on GB300: at head_dim
+// 128 it still wins with 4 tiles per warp (128 per unit, 32 warps); at 256
+// only with one (32 per unit; two already lost to stream-K).
+#ifndef FA_CL_MAX_TILES_128
+#define FA_CL_MAX_TILES_128 128
+#endif
+#ifndef FA_CL_MAX_TILES_256
+#define FA_CL_MAX_TILES_256 32
+#endif
+
+// Clusters of the cluster-plan kernel that fit on the current device at once
+// (cudaOccupancyMaxActiveClusters; 0 if the query fails), cached per device.
+template <int D, bool VI8>
+static int cluster_capacity()
+{
+    static std::mutex mu;
+    static int cache[64];
+    static bool done[64] = {false};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return 0;
+    std::lock_guard<std::mutex> lock(mu);
+    if (dev < 64 && done[dev])
+        return cache[dev];
+    const int smem = tc::Smem<D, VI8, 1>::BYTES;
+    int n = 0;
+    if (cudaFuncSetAttribute(tc::fa_stream_mma_kernel<D, VI8, false, 1, true>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem) == cudaSuccess) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(tc::CL_CTAS * 64);
+        cfg.blockDim = dim3(tc::Cfg<D, VI8>::NW * 32);
+        cfg.dynamicSmemBytes = smem;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = tc::CL_CTAS;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaOccupancyMaxActiveClusters(&n, tc::fa_stream_mma_kernel<D, VI8, false, 1, true>,
+                                           &cfg) != cudaSuccess)
+            n = 0;
+    }
+    cudaGetLastError();   // a refused query leaves no sticky error
+    if (dev < 64) {
+        cache[dev] = n;
+        done[dev] = true;
+    }
+    return n;
+}
+
+template <int D, bool VI8>
+static cudaError_t launch_cluster(const Params &p, const CUtensorMap &tmK, const CUtensorMap &tmV,
+                                  int units, cudaStream_t st)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(units * tc::CL_CTAS));
+    cfg.blockDim = dim3(tc::Cfg<D, VI8>::NW * 32);
+    cfg.dynamicSmemBytes = tc::Smem<D, VI8, 1>::BYTES;   // attribute set by cluster_capacity
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = tc::CL_CTAS;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, tc::fa_stream_mma_kernel<D, VI8, false, 1, true>, p,
+                                       tmK, tmV);
+    return e == cudaSuccess ? cudaGetLastError() : e;
+}
+
 static bool overlaps(const void *a, size_t na, const void *b, size_t nb)
 {
     if (!a || !b || na == 0 || nb == 0)
@@ -2932,6 +3186,25 @@ static int decode_impl(const void *q, const void *k_cache, const void *v_cache,
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const dim3 grid = pl.path == Path::Mma ? dim3(pl.ctas)
                                            : dim3(pl.max_splits, n_kv_heads * pl.n_hg, batch);
+    // Small steps take the cluster plan: a cluster per unit, partials folded
+    // in distributed shared memory, no merge kernel.  Only with one column
+    // group, when every unit's cluster fits on the GPU at once and a unit has
+    // at most FA_CL_MAX_TILES_<head_dim> tiles (FA_DECODE_PLAN=streamk turns
+    // it off).
+    bool cluster = false;
+    if (pl.path == Path::Mma && pl.chunk == 0 && pl.cpu == tc::GPH) {
+        const char *pe = getenv("FA_DECODE_PLAN");
+        const long long units_all = (long long)batch * pl.units;
+        const long long unit_tiles = ((ring ? cap + 16 : cap) + tc::TILE - 1) / tc::TILE;
+        const long long max_tiles = D == 128 ? FA_CL_MAX_TILES_128 : FA_CL_MAX_TILES_256;
+        if (!(pe && !strcmp(pe, "streamk")) && unit_tiles <= max_tiles) {
+            const int fit = D == 128 ? (vi8 ? cluster_capacity<128, true>()
+                                            : cluster_capacity<128, false>())
+                                     : (vi8 ? cluster_capacity<256, true>()
+                                            : cluster_capacity<256, false>());
+            cluster = units_all <= fit;
+        }
+    }
     cudaEvent_t prof_start = g_prof_start, prof_end = g_prof_end;
     g_prof_start = g_prof_end = nullptr;
     cudaError_t e = cudaSuccess;
@@ -2944,6 +3217,23 @@ static int decode_impl(const void *q, const void *k_cache, const void *v_cache,
         const int rk = encode_kv_map(&tmK, k_cache, kv_rows_total, D);
         if (rk)
             return rk;
+        if (cluster) {
+            if (vi8)
+                tmV = tmK;
+            else if (const int rv = encode_kv_map(&tmV, v_cache, kv_rows_total, D))
+                return rv;
+            const int units_all = batch * pl.units;
+            e = D == 128 ? (vi8 ? launch_cluster<128, true>(p, tmK, tmV, units_all, st)
+                                : launch_cluster<128, false>(p, tmK, tmV, units_all, st))
+                         : (vi8 ? launch_cluster<256, true>(p, tmK, tmV, units_all, st)
+                                : launch_cluster<256, false>(p, tmK, tmV, units_all, st));
+            if (e != cudaSuccess)
+                return fail(FA_ERR_CUDA, "fa_decode: cluster launch failed: %s",
+                            cudaGetErrorString(e));
+            if (prof_end && (e = cudaEventRecord(prof_end, st)) != cudaSuccess)
+                return fail(FA_ERR_CUDA, "fa_decode: profile event: %s", cudaGetErrorString(e));
+            return 0;     // the partials were folded in the kernel: no merge
+        }
         if (vi8) {
             tmV = tmK;   // unused: int8 V arrives by plain bulk copies
             if (pl.chunk > 0)

@@ -103,6 +103,18 @@ extern "C" {
  *
  * q, k_cache, v_cache, v_scales and out must be 16-byte aligned, and
  * seq_lens, block_table and window 4-byte aligned (else FA_ERR_ALIGN).
+ *
+ * Plans.  A step normally runs two kernels: a persistent split kernel that
+ * gives every warp an equal share of the step's tiles, then a log-sum-exp
+ * merge.  A small step -- one column group per KV head, at most 2048 tokens
+ * of capacity per sequence at head_dim 128 (512 at 256), and few enough
+ * (sequence, KV head) units that a cluster of 8 CTAs per unit fits on the
+ * GPU at once -- instead runs one
+ * kernel: each unit's cluster splits its tiles over its warps and folds their
+ * partials in distributed shared memory, so the workspace is not written.
+ * Setting FA_DECODE_PLAN=streamk in the environment keeps every step on the
+ * two-kernel plan.  Both plans compute the same result within the stated
+ * tolerances.
  */
 FA_API int fa_decode(const void *q, const void *k_cache, const void *v_cache,
                      const void *v_scales, const int32_t *block_table,

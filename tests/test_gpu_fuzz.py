@@ -6,7 +6,9 @@ contiguous, fp16 or int8 V) and an entry point: fa_decode, fa_decode_multi,
 fa_decode_ring and their batch-invariant forms.  Paged cases take pages of
 16, 32 or 64 tokens; a quarter of the single-query fa_decode and
 fa_decode_ring cases run on the CUDA-core split kernel (FA_DECODE_KERNEL=simt)
-instead of the tensor-core one.  A paged case outside the batch-invariant
+instead of the tensor-core one, and about a third of the rest hold the
+tensor-core kernel to the stream-K plan (FA_DECODE_PLAN=streamk) where the
+library would take the cluster plan of small steps.  A paged case outside the batch-invariant
 forms may take a block table of 2^20 tokens per sequence, which moves the
 planner to 16-column units when a KV head has more than 8 columns; batches of
 many rows reach the warp-per-row merge.  Unwritten cache rows and the
@@ -54,8 +56,12 @@ def _draw(seed):
     split = int(r.choice([16, 64, 256, 512]))
     P = int(r.choice([16, 16, 32, 64])) if paged else 16
     simt = mode in ("decode", "ring") and bool(r.random() < 0.25)
+    # the tensor-core kernel held to the stream-K plan in some cases that the
+    # library would give the cluster plan (drawn last: earlier draws unchanged)
+    streamk = bool(r.random() < 0.3)
     return dict(mode=mode, D=D, Hkv=Hkv, G=G, B=B, lens=lens, window=window, int8=int8,
-                paged=paged, big_cap=big_cap, tq=tq, split=split, P=P, simt=simt, seed=seed)
+                paged=paged, big_cap=big_cap, tq=tq, split=split, P=P, simt=simt,
+                streamk=streamk, seed=seed)
 
 
 def _ws(n):
@@ -162,25 +168,28 @@ def _run_ring(c):
 
 
 @contextlib.contextmanager
-def _split_kernel(simt):
-    """The library reads FA_DECODE_KERNEL at every call."""
-    old = os.environ.get("FA_DECODE_KERNEL")
+def _split_kernel(simt, streamk=False):
+    """The library reads FA_DECODE_KERNEL and FA_DECODE_PLAN at every call."""
+    old = {k: os.environ.get(k) for k in ("FA_DECODE_KERNEL", "FA_DECODE_PLAN")}
+    os.environ.pop("FA_DECODE_KERNEL", None)
+    os.environ.pop("FA_DECODE_PLAN", None)
     if simt:
         os.environ["FA_DECODE_KERNEL"] = "simt"
-    else:
-        os.environ.pop("FA_DECODE_KERNEL", None)
+    if streamk:
+        os.environ["FA_DECODE_PLAN"] = "streamk"
     try:
         yield
     finally:
-        if old is None:
-            os.environ.pop("FA_DECODE_KERNEL", None)
-        else:
-            os.environ["FA_DECODE_KERNEL"] = old
+        for k, v in old.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
 
 
 @pytest.mark.parametrize("seed", range(N_CASES))
 def test_random_case_matches_oracle(seed):
     c = _draw(seed)
-    with _split_kernel(c["simt"]):
+    with _split_kernel(c["simt"], c["streamk"]):
         got, want = (_run_ring if c["mode"].startswith("ring") else _run_paged_or_contig)(c)
     assert_close(got, want, c["int8"], str(c))

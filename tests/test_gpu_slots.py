@@ -16,9 +16,17 @@ pytestmark = pytest.mark.gpu
 N_SLOTS = 64
 
 
-@pytest.fixture(params=["mma", "simt"])
+@pytest.fixture(params=["mma", "mma_streamk", "simt"])
 def kernel(request, monkeypatch):
-    monkeypatch.setenv("FA_DECODE_KERNEL", request.param)
+    """Run a case through each split kernel and plan: the tensor-core kernel
+    with the plan the library picks (the cluster plan for small steps), the
+    tensor-core kernel held to the stream-K plan (FA_DECODE_PLAN=streamk), and
+    the CUDA-core kernel (FA_DECODE_KERNEL=simt); int8 V cases included."""
+    monkeypatch.setenv("FA_DECODE_KERNEL", "simt" if request.param == "simt" else "mma")
+    if request.param == "mma_streamk":
+        monkeypatch.setenv("FA_DECODE_PLAN", "streamk")
+    else:
+        monkeypatch.delenv("FA_DECODE_PLAN", raising=False)
     return request.param
 
 
