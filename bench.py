@@ -214,6 +214,21 @@ def call(wl, d, stream, out=None):
                       stream=stream)
 
 
+def l2_note(nbytes):
+    """How the timing protocol treats L2 for a step that reads `nbytes`."""
+    return ("flushed before every step: 512 MiB written, then 512 MiB read (clean lines)"
+            if nbytes < 4 * L2_BYTES else "inputs larger than 4x L2")
+
+
+def line_config(wl, nbytes, world):
+    """The `config` object of a JSON line: the same for both arms."""
+    from decode_step_kv_gb300.inputs import WORKLOAD_DESCRIPTIONS
+    return {"workload": f"{wl.name}: {WORKLOAD_DESCRIPTIONS[wl.name]}",
+            "batch": wl.batch, "n_q_heads": wl.n_q_heads, "n_kv_heads": wl.n_kv_heads,
+            "head_dim": wl.head_dim, "kv_bytes_per_step": nbytes, "l2": l2_note(nbytes),
+            "parallelism": f"replicas x{world} (no collectives)"}
+
+
 class L2Flush:
     """Leave L2 holding none of the step's data between timed steps: write a
     512 MiB buffer (evicts everything) and then reduce over another 512 MiB
@@ -239,8 +254,6 @@ def time_kernel(wl, d, steps, warmup, world, device, clocks_gpu=None):
     from decode_step_kv_gb300.inputs import kv_bytes
     nbytes = kv_bytes(wl, d["lens"], None if d["window"] is None else d["window"].tolist())
     flush = L2Flush(device) if nbytes < 4 * L2_BYTES else None
-    l2_note = ("flushed before every step: 512 MiB written, then 512 MiB read (clean lines)"
-               if flush else "inputs larger than 4x L2")
     stream = torch.cuda.current_stream(device)
     for i in range(warmup):
         if flush:
@@ -307,7 +320,7 @@ def time_kernel(wl, d, steps, warmup, world, device, clocks_gpu=None):
         "split_us": 1e3 * statistics.mean(split_ms),
         "kv_bytes": nbytes,
         "wall_s": wall,
-        "l2": l2_note,
+        "l2": l2_note(nbytes),
         "launches": 2 * steps,      # split + merge per timed step
     }
     if sampler:
@@ -724,10 +737,7 @@ def run_ours(args, world, rank, local):
                  "softmax; P rounded to fp16 for the PV product; fp16 K/V"
                  + (", int8 V x fp16 scale" if wl.v_int8 else "")),
         "data": "synthetic (seeded N(0,1) fp16 q/K/V, random block tables)",
-        "config": {"workload": f"{wl.name}: {WORKLOAD_DESCRIPTIONS[wl.name]}",
-                   "batch": wl.batch, "n_q_heads": wl.n_q_heads, "n_kv_heads": wl.n_kv_heads,
-                   "head_dim": wl.head_dim, "kv_bytes_per_step": r["kv_bytes"],
-                   "l2": r["l2"], "parallelism": f"replicas x{world} (no collectives)"},
+        "config": line_config(wl, r["kv_bytes"], world),
         "frac_of_hbm_peak": round(gbs_total / world / peak, 4),
         "roofline": {"bound": "hbm", "kernel": kernel,
                      "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
@@ -807,9 +817,14 @@ def run_reference(args, world, rank):
     """The fp64 CPU oracle, as it stands, on the host cores."""
     if rank != 0:
         return
-    from decode_step_kv_gb300.inputs import WORKLOADS, WORKLOAD_DESCRIPTIONS
+    from decode_step_kv_gb300.inputs import WORKLOADS, kv_bytes
     wl = WORKLOADS[args.workload]
     inp = cpu_inputs(wl)
+    # the K/V bytes of the workload's step (its lengths are fixed, or drawn
+    # with the inputs)
+    lens = inp.get("lens") or list(wl.seq_lens or ())
+    win = inp.get("window")
+    nbytes = kv_bytes(wl, lens, None if win is None else win.tolist())
     per_step_budget = max(0.2, 150.0 / max(1, args.steps + args.warmup))
     for _ in range(args.warmup):
         oracle_sample(wl, inp, budget_s=per_step_budget)
@@ -823,7 +838,7 @@ def run_reference(args, world, rank):
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": None, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": f"{wl.name}: {WORKLOAD_DESCRIPTIONS[wl.name]}"},
+            "config": line_config(wl, nbytes, world),
             "cpu_baseline": {"kind": "oracle", "cores": thr, "value": round(v, 4),
                              "unit": "GB/s",
                              "sample": f"per step: whole (sequence, kv-head) units of {wl.name} "
