@@ -3,8 +3,9 @@
 - The workspace needs no initialisation and may be reused, uncleared, across
   calls of other lengths and other shapes.
 - A call captured in a CUDA graph (its split kernel and the merge kernel
-  launched behind it with programmatic dependent launch) replays correctly
-  with new device-side lengths, since the split plan is made on the device.
+  launched behind it with programmatic dependent launch, or the one clustered
+  launch of a small step) replays correctly with new device-side lengths,
+  since the split plan is made on the device.
 """
 import zlib
 
@@ -66,13 +67,19 @@ def test_workspace_reused_across_calls_and_shapes():
         assert_close(out.cpu().numpy(), oracle_decode(wl, inp), False, f"call {i} ({wl.name})")
 
 
-@pytest.mark.parametrize("D,v_int8", [(128, False), (256, False), (256, True)])
-def test_graph_replay_with_new_lengths(D, v_int8):
+# the stream-K plan (split and merge kernels) and, at small capacities, the
+# cluster plan (one clustered launch)
+GRAPH_CASES = [(128, False, [4000, 2600, 1500, 3100]), (256, False, [4000, 2600, 1500, 3100]),
+               (256, True, [4000, 2600, 1500, 3100]), (128, False, [2000, 1300, 700, 1500]),
+               (128, True, [2000, 1300, 700, 1500]), (256, False, [500, 300, 100, 512])]
+
+
+@pytest.mark.parametrize("D,v_int8,full", GRAPH_CASES)
+def test_graph_replay_with_new_lengths(D, v_int8, full):
     """A launch captured in a CUDA graph replays with the lengths the device
     holds at replay time; each replay matches the oracle for those lengths."""
-    wl = W(f"graph_{D}_{int(v_int8)}", 4, 8, 2, D, paged=True, v_int8=v_int8, window=700,
-           window_odd_only=True)
-    full = [4000, 2600, 1500, 3100]
+    wl = W(f"graph_{D}_{int(v_int8)}_{max(full)}", 4, 8, 2, D, paged=True, v_int8=v_int8,
+           window=700, window_odd_only=True)
     inp = build_case(wl, seq_lens=full, spare_blocks=2)
     dinp = to_cuda(inp)
     cap = dinp["max_blocks"] * wl.page_size
@@ -86,8 +93,7 @@ def test_graph_replay_with_new_lengths(D, v_int8):
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=s):
         _call(wl, dinp, ws, out, stream=s)
-    for lens in ([4000, 2600, 1500, 3100], [1, 2599, 0, 3000], [3999, 16, 1500, 17],
-                 [4000, 2600, 1500, 3100]):
+    for lens in (full, [1, full[1] - 1, 0, full[3] - 100], [full[0] - 1, 16, full[2], 17], full):
         dinp["seq_lens"].copy_(torch.tensor(lens, dtype=torch.int32))
         out.fill_(float("nan"))
         g.replay()
