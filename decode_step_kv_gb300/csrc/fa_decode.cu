@@ -50,6 +50,7 @@
 #include <string.h>
 
 #include <mutex>
+#include <type_traits>
 #include <utility>
 #include <stdlib.h>
 
@@ -112,6 +113,7 @@ struct Params {
     const int *slot;  // contiguous / ring caches: sequence b's cache is slot slot[b] of
                       // [n_slots][Hkv][cap][D]; NULL: slot b
     int n_slots;
+    int cl_ctas;      // cluster plan: CTAs per cluster (1, 2, 4 or 8)
 };
 
 // ------------------------------------------------------------ PTX wrappers
@@ -1131,10 +1133,11 @@ __device__ __forceinline__ void column_range(const Params &p, int b, int L, int 
 // groups of 8 (query, head) columns a warp carries per K/V tile; 2 lets a
 // unit hold 16 columns, so more than 8 columns per KV head read each tile
 // once instead of once per group.  CL: the cluster plan for small steps --
-// one thread-block cluster of CL_CTAS CTAs per unit, the unit's tiles split
-// evenly over the cluster's warps, and the warps' partials folded through
-// distributed shared memory at the end, so no merge kernel runs.
-constexpr int CL_CTAS = 8;      // CTAs per cluster (the portable maximum)
+// one thread-block cluster of p.cl_ctas CTAs per unit (1, 2, 4 or 8), the
+// unit's tiles split evenly over the cluster's warps, and the warps' partials
+// folded through distributed shared memory at the end, so no merge kernel
+// runs.
+constexpr int CL_MAX_CTAS = 8;  // the portable maximum cluster size
 template <int D, bool VI8, bool BI, int NG, bool CL = false>
 __global__ void __launch_bounds__(Cfg<D, VI8, NG>::NW * 32, 1)
     fa_stream_mma_kernel(const Params p, const __grid_constant__ CUtensorMap tmK,
@@ -1165,16 +1168,17 @@ __global__ void __launch_bounds__(Cfg<D, VI8, NG>::NW * 32, 1)
     int cl_j = 0, cl_n = 0;           // cluster plan: the cluster's unit and its tiles
     if constexpr (CL) {
         // cluster plan: unit u = cluster index; worker r of the cluster's
-        // CL_CTAS x NW warps takes tiles [r*n/R, (r+1)*n/R) of it.  No warp
-        // leaves early: every thread must reach the cluster barriers below.
-        const int u = blockIdx.x / CL_CTAS;
+        // R = cl_ctas x NW warps takes tiles [r*n/R, (r+1)*n/R) of it.  No
+        // warp leaves early: every thread must reach the cluster barriers.
+        const int cs = p.cl_ctas;
+        const int u = blockIdx.x / cs;
         b_at = u / p.U_b;
         cl_j = u % p.U_b;
         int lo, hi;
-        attended_range(p, b_at, lo, hi, blockIdx.x % CL_CTAS == 0 && threadIdx.x == 0);
+        attended_range(p, b_at, lo, hi, blockIdx.x % cs == 0 && threadIdx.x == 0);
         cl_n = tiles_in<TILE>(lo, hi);
-        constexpr int R = CL_CTAS * C::NW;
-        const int r = (blockIdx.x % CL_CTAS) * C::NW + warp;
+        const int R = cs * C::NW;
+        const int r = (blockIdx.x % cs) * C::NW + warp;
         t0 = (long long)r * cl_n / R;
         t1 = (long long)(r + 1) * cl_n / R;
         P_at = -(long long)cl_j * cl_n;   // positions count from the unit's first tile
@@ -1755,12 +1759,12 @@ __global__ void __launch_bounds__(Cfg<D, VI8, NG>::NW * 32, 1)
         cluster_sync();
         uint32_t rank;
         asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(rank));
-        // column c of the unit: warp c / CL_CTAS of cluster CTA c % CL_CTAS
-        const int c = warp * CL_CTAS + static_cast<int>(rank);
-        if (c < nh) {
-            constexpr int R = CL_CTAS * C::NW;          // partials: one per warp of the cluster
-            static_assert(R % 8 == 0, "partials come in batches of 8");
-            constexpr int PPL = (R + 31) / 32;          // partials per lane
+        // column c of the unit: warp (c / cl_ctas) mod NW of cluster CTA
+        // c % cl_ctas (one pass when the cluster has 8 warps or more, two
+        // with a single 4-warp CTA)
+        const int R = p.cl_ctas * C::NW;                // partials: one per warp of the cluster
+        for (int c = warp * p.cl_ctas + static_cast<int>(rank); c < nh; c += R) {
+            constexpr int PPL = (CL_MAX_CTAS * C::NW + 31) / 32;   // partials per lane, at most
             constexpr int EPL2 = D / 32;                // output floats per lane
             float wv[PPL], Lsum = 0.f, M = -INFINITY;
             float mv[PPL], lv[PPL];
@@ -1793,13 +1797,15 @@ __global__ void __launch_bounds__(Cfg<D, VI8, NG>::NW * 32, 1)
 #pragma unroll
             for (int e = 0; e < EPL2; ++e)
                 o[e] = 0.f;
-            // eight partials' loads in flight before their sums (empty
-            // partials hold zeros and weigh 0)
-            constexpr int BATCH = 8;
-            for (int i0 = 0; i0 < R; i0 += BATCH) {
-                float4 x[BATCH][EPL2 / 4];
+            // NB partials' loads in flight before their sums (empty partials
+            // hold zeros and weigh 0): batches of 8, and one of 4 when the
+            // cluster is a single 4-warp CTA.  Each batch is unrolled, so the
+            // weights are picked by a select, never by a runtime index.
+            auto fold = [&](const int i0, auto nb) {
+                constexpr int NB = decltype(nb)::value;
+                float4 x[NB][EPL2 / 4];
 #pragma unroll
-                for (int u = 0; u < BATCH; ++u) {
+                for (int u = 0; u < NB; ++u) {
                     const int i = i0 + u;
                     const uint32_t src = cl_map(base + (i % C::NW) * C::WARP_BYTES +
                                                     (c * D + lane * EPL2) * 4,
@@ -1809,9 +1815,10 @@ __global__ void __launch_bounds__(Cfg<D, VI8, NG>::NW * 32, 1)
                         x[u][e] = cl_ld4(src + e * 16);
                 }
 #pragma unroll
-                for (int u = 0; u < BATCH; ++u) {
+                for (int u = 0; u < NB; ++u) {
                     const int i = i0 + u;
-                    const float a = __shfl_sync(0xffffffffu, wv[i / 32], i % 32);
+                    const float wsel = (PPL > 1 && i >= 32) ? wv[PPL - 1] : wv[0];
+                    const float a = __shfl_sync(0xffffffffu, wsel, i % 32);
 #pragma unroll
                     for (int e = 0; e < EPL2 / 4; ++e) {
                         o[4 * e] = fmaf(x[u][e].x, a, o[4 * e]);
@@ -1820,7 +1827,12 @@ __global__ void __launch_bounds__(Cfg<D, VI8, NG>::NW * 32, 1)
                         o[4 * e + 3] = fmaf(x[u][e].w, a, o[4 * e + 3]);
                     }
                 }
-            }
+            };
+            int i0 = 0;
+            for (; i0 + 8 <= R; i0 += 8)
+                fold(i0, std::integral_constant<int, 8>());
+            if (i0 < R)                              // R is a multiple of 4
+                fold(i0, std::integral_constant<int, 4>());
             const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
             const Col cq = column(p, cl_j / p.n_hg, cl_j % p.n_hg, c, CPU);
             float4 *dst = reinterpret_cast<float4 *>(
@@ -2669,43 +2681,45 @@ static cudaError_t launch_mma(const Params &p, const CUtensorMap &tmK, const CUt
     return cudaGetLastError();
 }
 
-// Cluster plan (tc::CL_CTAS CTAs per unit, no merge kernel): the largest
-// unit it takes, in 16-token tiles, beyond which the stream-K plan's use of
-// every SM wins over saving the merge kernel.  Measured on GB300: at head_dim
-// 128 it still wins with 4 tiles per warp (128 per unit, 32 warps); at 256
-// only with one (32 per unit; two already lost to stream-K).
-#ifndef FA_CL_MAX_TILES_128
-#define FA_CL_MAX_TILES_128 128
+// Cluster plan (a cluster of 2, 4 or 8 CTAs per unit, no merge kernel): the
+// most tiles per warp it takes, beyond which the stream-K plan's use of every
+// SM wins over saving the merge kernel.  Measured on GB300: at head_dim 128
+// it still wins with 4 tiles per warp and not with 8; at 256 with one and
+// not with two.
+#ifndef FA_CL_MAX_TPW_128
+#define FA_CL_MAX_TPW_128 4
 #endif
-#ifndef FA_CL_MAX_TILES_256
-#define FA_CL_MAX_TILES_256 32
+#ifndef FA_CL_MAX_TPW_256
+#define FA_CL_MAX_TPW_256 1
 #endif
 
-// Clusters of the cluster-plan kernel that fit on the current device at once
-// (cudaOccupancyMaxActiveClusters; 0 if the query fails), cached per device.
+// Clusters of `cs` CTAs of the cluster-plan kernel that fit on the current
+// device at once (cudaOccupancyMaxActiveClusters; 0 if the query fails),
+// cached per device and cluster size.
 template <int D, bool VI8>
-static int cluster_capacity()
+static int cluster_capacity(int cs)
 {
     static std::mutex mu;
-    static int cache[64];
-    static bool done[64] = {false};
+    static int cache[64][4];
+    static bool done[64][4] = {};
+    const int ci = cs == 1 ? 0 : cs == 2 ? 1 : cs == 4 ? 2 : 3;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess)
         return 0;
     std::lock_guard<std::mutex> lock(mu);
-    if (dev < 64 && done[dev])
-        return cache[dev];
+    if (dev < 64 && done[dev][ci])
+        return cache[dev][ci];
     const int smem = tc::Smem<D, VI8, 1>::BYTES;
     int n = 0;
     if (cudaFuncSetAttribute(tc::fa_stream_mma_kernel<D, VI8, false, 1, true>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, smem) == cudaSuccess) {
         cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(tc::CL_CTAS * 64);
+        cfg.gridDim = dim3(cs * 64);
         cfg.blockDim = dim3(tc::Cfg<D, VI8>::NW * 32);
         cfg.dynamicSmemBytes = smem;
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = tc::CL_CTAS;
+        attr[0].val.clusterDim.x = cs;
         attr[0].val.clusterDim.y = 1;
         attr[0].val.clusterDim.z = 1;
         cfg.attrs = attr;
@@ -2716,8 +2730,8 @@ static int cluster_capacity()
     }
     cudaGetLastError();   // a refused query leaves no sticky error
     if (dev < 64) {
-        cache[dev] = n;
-        done[dev] = true;
+        cache[dev][ci] = n;
+        done[dev][ci] = true;
     }
     return n;
 }
@@ -2727,13 +2741,13 @@ static cudaError_t launch_cluster(const Params &p, const CUtensorMap &tmK, const
                                   int units, cudaStream_t st)
 {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(units * tc::CL_CTAS));
+    cfg.gridDim = dim3(static_cast<unsigned>(units * p.cl_ctas));
     cfg.blockDim = dim3(tc::Cfg<D, VI8>::NW * 32);
     cfg.dynamicSmemBytes = tc::Smem<D, VI8, 1>::BYTES;   // attribute set by cluster_capacity
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = tc::CL_CTAS;
+    attr[0].val.clusterDim.x = p.cl_ctas;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
@@ -3207,23 +3221,32 @@ static int decode_impl(const void *q, const void *k_cache, const void *v_cache,
                                            : dim3(pl.max_splits, n_kv_heads * pl.n_hg, batch);
     // Small steps take the cluster plan: a cluster per unit, partials folded
     // in distributed shared memory, no merge kernel.  Only with one column
-    // group, when every unit's cluster fits on the GPU at once and a unit has
-    // at most FA_CL_MAX_TILES_<head_dim> tiles (FA_DECODE_PLAN=streamk turns
-    // it off).
-    bool cluster = false;
+    // group, and with the largest cluster (8, 4, 2 or 1 CTAs) for which every
+    // unit's cluster fits on the GPU at once and a warp gets at most
+    // FA_CL_MAX_TPW_<head_dim> tiles (FA_DECODE_PLAN=streamk turns it off).
+    int cluster_ctas = 0;
     if (pl.path == Path::Mma && pl.chunk == 0 && pl.cpu == tc::GPH) {
         const char *pe = getenv("FA_DECODE_PLAN");
         const long long units_all = (long long)batch * pl.units;
         const long long unit_tiles = ((ring ? cap + 16 : cap) + tc::TILE - 1) / tc::TILE;
-        const long long max_tiles = D == 128 ? FA_CL_MAX_TILES_128 : FA_CL_MAX_TILES_256;
-        if (!(pe && !strcmp(pe, "streamk")) && unit_tiles <= max_tiles) {
-            const int fit = D == 128 ? (vi8 ? cluster_capacity<128, true>()
-                                            : cluster_capacity<128, false>())
-                                     : (vi8 ? cluster_capacity<256, true>()
-                                            : cluster_capacity<256, false>());
-            cluster = units_all <= fit;
+        const int nw = D == 128 ? (vi8 ? tc::Cfg<128, true>::NW : tc::Cfg<128, false>::NW)
+                                : (vi8 ? tc::Cfg<256, true>::NW : tc::Cfg<256, false>::NW);
+        const long long max_tpw = D == 128 ? FA_CL_MAX_TPW_128 : FA_CL_MAX_TPW_256;
+        for (int cs = tc::CL_MAX_CTAS; cs >= 1 && !(pe && !strcmp(pe, "streamk")); cs /= 2) {
+            if ((unit_tiles + (long long)cs * nw - 1) / ((long long)cs * nw) > max_tpw)
+                break;                       // smaller clusters give each warp more
+            const int fit = D == 128 ? (vi8 ? cluster_capacity<128, true>(cs)
+                                            : cluster_capacity<128, false>(cs))
+                                     : (vi8 ? cluster_capacity<256, true>(cs)
+                                            : cluster_capacity<256, false>(cs));
+            if (units_all <= fit) {
+                cluster_ctas = cs;
+                break;
+            }
         }
     }
+    const bool cluster = cluster_ctas > 0;
+    p.cl_ctas = cluster_ctas;
     cudaEvent_t prof_start = g_prof_start, prof_end = g_prof_end;
     g_prof_start = g_prof_end = nullptr;
     cudaError_t e = cudaSuccess;

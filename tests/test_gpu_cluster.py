@@ -32,6 +32,14 @@ CASES = [
     # one query head per KV head, and eight
     (W("mha", 2, 4, 4, 128, seed=36), [33, 250]),
     (W("gqa8", 2, 16, 2, 128, paged=True, window=64, seed=37), [1024, 65]),
+    # more units than 8-CTA clusters fit: 4-CTA clusters (64 units), then 2-CTA
+    # clusters (128 units), each warp still at most 4 tiles
+    (W("clusters_of_4", 8, 32, 8, 128, paged=True, seed=39), [1000, 3, 512, 1024, 0, 77, 640, 999]),
+    (W("clusters_of_2", 16, 32, 8, 128, seed=40), [512, 1, 300, 17, 480, 512, 0, 256,
+                                                   100, 511, 64, 33, 200, 400, 16, 500]),
+    # 256 units of at most 16 tiles: one-CTA clusters, the columns folded in two passes
+    (W("clusters_of_1", 32, 32, 8, 128, paged=True, window=100, window_odd_only=True, seed=41),
+     [256, 1, 0, 17, 255, 128, 64, 200] * 4),
 ]
 
 
