@@ -106,12 +106,12 @@ extern "C" {
  *
  * Plans.  A step normally runs two kernels: a persistent split kernel that
  * gives every warp an equal share of the step's tiles, then a log-sum-exp
- * merge.  A small step -- one column group per KV head, at most 2048 tokens
- * of capacity per sequence at head_dim 128 (512 at 256), and few enough
- * (sequence, KV head) units that a cluster of 8 CTAs per unit fits on the
- * GPU at once -- instead runs one
- * kernel: each unit's cluster splits its tiles over its warps and folds their
- * partials in distributed shared memory, so the workspace is not written.
+ * merge.  A small step -- one column group per KV head, and few and short
+ * enough (sequence, KV head) units that a thread-block cluster of 8, 4, 2 or 1
+ * CTAs per unit fits on the GPU at once with at most 4 tiles of 16 tokens per
+ * warp at head_dim 128 (1 at 256) -- instead runs one kernel: each unit's
+ * cluster splits its tiles over its warps and folds their partials in
+ * distributed shared memory, so the workspace is not written.
  * Setting FA_DECODE_PLAN=streamk in the environment keeps every step on the
  * two-kernel plan.  Both plans compute the same result within the stated
  * tolerances.
