@@ -2725,10 +2725,13 @@ static int cluster_capacity(int cs)
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         if (cudaOccupancyMaxActiveClusters(&n, tc::fa_stream_mma_kernel<D, VI8, false, 1, true>,
-                                           &cfg) != cudaSuccess)
+                                           &cfg) != cudaSuccess) {
             n = 0;
+            cudaGetLastError();   // clear the error this refused query left (and only then)
+        }
+    } else {
+        cudaGetLastError();       // likewise for a refused attribute
     }
-    cudaGetLastError();   // a refused query leaves no sticky error
     if (dev < 64) {
         cache[dev][ci] = n;
         done[dev][ci] = true;
