@@ -944,12 +944,6 @@ struct Walk {
         return P + (long long)j * (n + c) + c;
     }
     __device__ __forceinline__ long long pos() const { return unit_start() + k; }
-    // whether the next tile (the following unit's first at a unit's end) lies
-    // at or beyond flattened position t1
-    __device__ __forceinline__ bool last_before(long long t1) const
-    {
-        return pos() + 1 + (k == n - 1 ? c : 0) >= t1;
-    }
 };
 
 // Warp-cooperative scan over the sequences: T = the flattened positions of
