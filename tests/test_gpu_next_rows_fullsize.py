@@ -1,7 +1,8 @@
 """Parity at the sizes the benchmark times for the rows beyond the plain
 decode step: multi-query decode (4 queries) and the batch-invariant plan on
-the 32 x 32K, 32/8-head, D=128 paged workload, and ring decode on 64
-sequences with 64x128-64k_d128_win's heads and lengths over 4096-row rings.  The oracle
+the 32 x 32K, 32/8-head, D=128 paged workload, ring decode on 64 sequences
+with 64x128-64k_d128_win's heads and lengths over 4096-row rings, and the slot
+map over a pool of 64 contiguous 16K caches.  The oracle
 recomputes a sample of the sequences (every output row of each), each from a
 host copy of that sequence's cache alone.
 """
@@ -109,5 +110,39 @@ def test_ring_decode_at_bench_size():
                                   d["v_cache"][b:b + 1].cpu().numpy(), [d["lens"][b]],
                                   scale=wl.scale, n_kv_heads=Hkv)
         assert_close(got[b:b + 1], want, False, f"ring sequence {b} ({d['lens'][b]} tokens)")
+    del d
+    torch.cuda.empty_cache()
+
+
+def test_slot_map_eight_of_sixty_four_at_full_size():
+    """The benchmark's slot-map row: 8 active slots (a seeded permutation) of a
+    64-slot pool of contiguous 16K caches, 32 q / 8 kv heads, D=128.  The
+    oracle decodes each sampled row from a host copy of its slot alone (a
+    slot map equals the gathered sub-batch)."""
+    n_slots, C = 64, 16384
+    wl = dataclasses.replace(WORKLOADS["32x32k_d128_paged"], name="slots", batch=n_slots,
+                             paged=False, seq_lens=(C,) * n_slots)
+    torch.cuda.empty_cache()
+    d = make_inputs(wl, "cuda", capacity=C)
+    B, Hq, Hkv, D = 8, wl.n_q_heads, wl.n_kv_heads, wl.head_dim
+    g = torch.Generator(device="cpu").manual_seed(wl.seed + 3000)
+    active = torch.randperm(n_slots, generator=g)[:B].to(torch.int32)
+    lens = [C, C - 1, 1, 5000, C, 77, 12345, C]          # ragged within the slots' caches
+    q8 = d["q"][:B].contiguous()
+    ws = torch.full((max(binding.fa_decode_workspace_size(B, Hq, Hkv, D, C), 16),), 0xFF,
+                    dtype=torch.uint8, device="cuda")
+    out = torch.full((B, Hq, D), float("nan"), device="cuda")
+    binding.fa_decode_slots(q8, d["k_cache"], d["v_cache"], None, active.cuda(),
+                            torch.tensor(lens, dtype=torch.int32, device="cuda"), Hq, Hkv, D,
+                            wl.scale, None, out, workspace=ws)
+    got = out.cpu().numpy()
+    for b in _sample(B):
+        s, L = int(active[b]), lens[b]
+        k = d["k_cache"][s:s + 1, :, :L].contiguous().cpu().numpy()
+        v = d["v_cache"][s:s + 1, :, :L].contiguous().cpu().numpy()
+        want = oracle.decode(q8[b:b + 1].cpu().numpy(), k, v, [L], scale=wl.scale,
+                             n_kv_heads=Hkv)
+        assert_close(got[b:b + 1], want, False, f"slot {s} (row {b}, {L} keys)")
+    assert np.all(np.isfinite(got))
     del d
     torch.cuda.empty_cache()
