@@ -499,6 +499,27 @@ def time_next_rows(steps, device, peak):
     del d2, q, ws, out
     torch.cuda.empty_cache()
 
+    # the same with 16x16k_d256_int8v's own int8 V
+    wl3 = WORKLOADS["16x16k_d256_int8v"]
+    d3 = prepare(wl3, device)
+    nbytes3 = kv_bytes(wl3, d3["lens"], None)
+    q = make_queries(wl3, 8, device)
+    n = binding.fa_decode_multi_workspace_size(B2, 8, Hq2, Hkv2, D2,
+                                               d3["max_blocks"] * wl3.page_size)
+    ws = torch.empty(max(n, 16), dtype=torch.uint8, device=device)
+    out = torch.empty((B2, 8, Hq2, D2), dtype=torch.float32, device=device)
+    us = time_steps(lambda: binding.fa_decode_multi(
+        q, d3["k_cache"], d3["v_cache"], d3["v_scales"], d3["block_table"], d3["seq_lens"], Hq2,
+        Hkv2, D2, wl3.scale, None, out, max_blocks_per_seq=d3["max_blocks"],
+        num_blocks=d3["num_blocks"], workspace=ws, stream=stream), nbytes3, steps, 3, device)
+    gbs = nbytes3 / (us * 1e-6) / 1e9
+    res["multi_query_d256_int8_tq8"] = {
+        "workload": "16x16k_d256_int8v (16 x 16K, 16 q/8 kv heads, D=256, paged, int8 V), "
+                    "8 queries per sequence", "us_per_step": round(us, 2), "kv_bytes": nbytes3,
+        "GB/s": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4), "column_groups": 2}
+    del d3, q, ws, out
+    torch.cuda.empty_cache()
+
     # cache append: one new K/V row per (sequence, KV head) at each sequence's
     # last position, into 32x32k_d128_paged's paged cache (fp16 V) and 16x16k_d256_int8v's (int8 V)
     g = torch.Generator(device=device)

@@ -708,11 +708,19 @@ constexpr int GPH = 8;          // heads per unit (the mma N dimension)
 #define FA_TC_STAGES_256_NG2 2
 #endif
 
+// head_dim 256, int8 V, two column groups per warp: the most warps whose
+// rings (2 stages) and query rows fit; 6 warps measured 15% faster than 5 and
+// than the single-group kernel on 8-query decode (16 x 16K, 16 q / 8 kv heads)
+#ifndef FA_TC_NW_256_I8_NG2
+#define FA_TC_NW_256_I8_NG2 6
+#endif
+
 template <int D, bool VI8, int NG = 1>
 struct Cfg {
     static constexpr bool TWO256 = D == 256 && !VI8 && NG == 2;
+    static constexpr bool TWO256_I8 = D == 256 && VI8 && NG == 2;
     static constexpr int NW = D == 128 ? FA_TC_NW_128
-                                       : (VI8 ? FA_TC_NW_256_I8
+                                       : (VI8 ? (TWO256_I8 ? FA_TC_NW_256_I8_NG2 : FA_TC_NW_256_I8)
                                               : (TWO256 ? FA_TC_NW_256_NG2 : FA_TC_NW_256));
     static constexpr int STAGES =
         D == 128 ? FA_TC_STAGES_128
@@ -736,8 +744,7 @@ struct Cfg {
 
 // Shared memory of the stream-K kernel: the rings and barriers, plus, when
 // two column groups ride a warp at D=256 (QSM), each warp's 16 query rows,
-// kept there instead of in registers (with int8 V at D=256 they do not fit,
-// so that kernel keeps one group).
+// kept there instead of in registers.
 template <int D, bool VI8, int NG>
 struct Smem {
     static constexpr bool QSM = D == 256 && NG == 2;
@@ -2435,11 +2442,10 @@ static Plan make_plan(Path path, int B, int Hq, int Hkv, int D, long long cap, i
         // step streams from HBM; on a step whose K/V fits in L2 the second
         // group's re-read hits L2 and the single-group units keep twice the
         // warps busy, so the choice goes by the K/V the capacity allows.
-        // int8 V at D=256 has no room for two groups; the batch-invariant
-        // plan keeps 8.
+        // The batch-invariant plan keeps 8.
         const double kv_bound = (double)B * (double)cap * Hkv *
                                 (2.0 * D + (vi8 ? D + D / 16.0 : 2.0 * D));
-        pl.cpu = ((D == 128 || !vi8) && chunk == 0 && tq * G > tc::GPH &&
+        pl.cpu = (chunk == 0 && tq * G > tc::GPH &&
                   kv_bound >= TWO_GROUP_MIN_KV_BYTES)
                      ? 2 * tc::GPH
                      : tc::GPH;
@@ -2450,6 +2456,9 @@ static Plan make_plan(Path path, int B, int Hq, int Hkv, int D, long long cap, i
         if (D == 128) {
             nw = vi8 ? tc::Cfg<128, true>::NW : tc::Cfg<128, false>::NW;
             cps = vi8 ? tc::Cfg<128, true>::CTAS_PER_SM : tc::Cfg<128, false>::CTAS_PER_SM;
+        } else if (vi8 && pl.cpu > tc::GPH) {
+            nw = tc::Cfg<256, true, 2>::NW;
+            cps = tc::Cfg<256, true, 2>::CTAS_PER_SM;
         } else if (vi8) {
             nw = tc::Cfg<256, true>::NW;
             cps = tc::Cfg<256, true>::CTAS_PER_SM;
@@ -3279,7 +3288,8 @@ static int decode_impl(const void *q, const void *k_cache, const void *v_cache,
                 e = D == 128 ? launch_mma<128, true, true>(p, tmK, tmV, grid, st)
                              : launch_mma<256, true, true>(p, tmK, tmV, grid, st);
             else if (pl.cpu > tc::GPH)
-                e = launch_mma<128, true, false, 2>(p, tmK, tmV, grid, st);   // D = 128 only
+                e = D == 128 ? launch_mma<128, true, false, 2>(p, tmK, tmV, grid, st)
+                             : launch_mma<256, true, false, 2>(p, tmK, tmV, grid, st);
             else
                 e = D == 128 ? launch_mma<128, true, false>(p, tmK, tmV, grid, st)
                              : launch_mma<256, true, false>(p, tmK, tmV, grid, st);

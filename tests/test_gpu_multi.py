@@ -38,8 +38,8 @@ CASES = [
 
 # The same kind of cases with a block table of 2^20 tokens per sequence: the
 # K/V the capacity allows passes the two-column-group threshold, so units
-# hold 16 columns (at D=256 with the query rows in shared memory), while the
-# pool holds only the blocks the lengths need.
+# hold 16 columns (at D=256 with the query rows in shared memory, fp16 or int8
+# V), while the pool holds only the blocks the lengths need.
 BIG_CAP = 1 << 20
 CASES_TWO_GROUPS = [
     ("2g_g4_tq4_window", 3, 8, 2, 128, 4, 5, True, False, [100, 1000, 40]),
@@ -48,6 +48,8 @@ CASES_TWO_GROUPS = [
     ("2g_d256_tq8", 3, 4, 2, 256, 8, 0, True, False, [900, 2000, 5]),
     ("2g_d256_tq6_window", 2, 4, 2, 256, 6, 50, True, False, [300, 64]),
     ("2g_d256_tq7_ragged", 5, 8, 2, 256, 7, 0, True, False, [1, 7, 33, 1500, 4000]),
+    ("2g_d256_tq8_int8", 3, 4, 2, 256, 8, 0, True, True, [900, 2000, 5]),
+    ("2g_d256_tq5_int8_window", 4, 8, 2, 256, 5, 40, True, True, [1, 300, 2500, 64]),
 ]
 
 
