@@ -382,7 +382,8 @@ def time_steps(step, nbytes, steps, warmup, device):
 def time_next_rows(steps, device, peak):
     """The rows beyond the plain decode step, each timed under the headline's
     protocol on seeded inputs of the decode shapes: ring-cache decode,
-    slot-map decode, multi-query decode, cache append."""
+    slot-map decode, multi-query decode, int8 V at head_dim 128, cache
+    append."""
     import torch
     from decode_step_kv_gb300 import binding
     from decode_step_kv_gb300.inputs import WORKLOADS, kv_bytes, make_inputs, make_queries
@@ -518,6 +519,28 @@ def time_next_rows(steps, device, peak):
                     "8 queries per sequence", "us_per_step": round(us, 2), "kv_bytes": nbytes3,
         "GB/s": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4), "column_groups": 2}
     del d3, q, ws, out
+    torch.cuda.empty_cache()
+
+    # int8 V at head_dim 128: 32x32k_d128_paged's shape with its V packed to int8
+    wl4 = dataclasses.replace(WORKLOADS["32x32k_d128_paged"], name="32x32k_d128_paged_int8v",
+                              v_int8=True)
+    d4 = prepare(wl4, device)
+    B4, Hq4, Hkv4, D4 = wl4.batch, wl4.n_q_heads, wl4.n_kv_heads, wl4.head_dim
+    nbytes4 = kv_bytes(wl4, d4["lens"], None)
+    ws = binding.alloc_workspace(B4, Hq4, Hkv4, D4, d4["max_blocks"] * wl4.page_size,
+                                 device=device)
+    out = torch.empty((B4, Hq4, D4), dtype=torch.float32, device=device)
+    us = time_steps(lambda: binding.fa_decode(
+        d4["q"], d4["k_cache"], d4["v_cache"], d4["v_scales"], d4["block_table"], d4["seq_lens"],
+        Hq4, Hkv4, D4, wl4.scale, None, out, batch=B4, page_size=wl4.page_size,
+        max_blocks_per_seq=d4["max_blocks"], num_blocks=d4["num_blocks"], workspace=ws,
+        stream=stream), nbytes4, steps, 3, device)
+    gbs = nbytes4 / (us * 1e-6) / 1e9
+    res["int8v_d128"] = {
+        "workload": "32x32k_d128_paged with int8 V (32 x 32K, 32 q/8 kv heads, D=128, paged)",
+        "us_per_step": round(us, 2), "kv_bytes": nbytes4, "GB/s": round(gbs, 1),
+        "frac_of_peak": round(gbs / peak, 4)}
+    del d4, ws, out
     torch.cuda.empty_cache()
 
     # cache append: one new K/V row per (sequence, KV head) at each sequence's

@@ -664,7 +664,8 @@ constexpr int GPH = 8;          // heads per unit (the mma N dimension)
 // head_dim 128 takes 2 CTAs x 4 warps x 3 stages (~100 KB each); head_dim 256
 // with fp16 V takes 4 warps x 3 stages of 16 KB; with int8 V the per-tile
 // dequantisation wants warps to switch between, so V is dequantised in place
-// over the consumed K tile and the freed memory buys 8 warps x 2 stages.
+// over the consumed K tile and the freed memory buys more warps: 8 x 2 stages
+// at head_dim 256, 3 CTAs x 4 warps x 2 stages at 128.
 #ifndef FA_TC_NW_128
 #define FA_TC_NW_128 4
 #endif
@@ -673,6 +674,19 @@ constexpr int GPH = 8;          // heads per unit (the mma N dimension)
 #endif
 #ifndef FA_TC_CTAS_128
 #define FA_TC_CTAS_128 2
+#endif
+// head_dim 128 with int8 V: 3 CTAs x 4 warps x 2 stages of 7 KB, at most 168
+// registers a thread; the 12 warps per SM measured 22-27% faster than 2 x 4 x 3
+// on 16K-token steps (one and two queries), 2 x 6 x 2 as fast, 3 x 5 x 2 (128
+// registers) slower
+#ifndef FA_TC_NW_128_I8
+#define FA_TC_NW_128_I8 4
+#endif
+#ifndef FA_TC_STAGES_128_I8
+#define FA_TC_STAGES_128_I8 2
+#endif
+#ifndef FA_TC_CTAS_128_I8
+#define FA_TC_CTAS_128_I8 3
 #endif
 #ifndef FA_TC_NW_256
 #define FA_TC_NW_256 4
@@ -719,11 +733,11 @@ template <int D, bool VI8, int NG = 1>
 struct Cfg {
     static constexpr bool TWO256 = D == 256 && !VI8 && NG == 2;
     static constexpr bool TWO256_I8 = D == 256 && VI8 && NG == 2;
-    static constexpr int NW = D == 128 ? FA_TC_NW_128
+    static constexpr int NW = D == 128 ? (VI8 ? FA_TC_NW_128_I8 : FA_TC_NW_128)
                                        : (VI8 ? (TWO256_I8 ? FA_TC_NW_256_I8_NG2 : FA_TC_NW_256_I8)
                                               : (TWO256 ? FA_TC_NW_256_NG2 : FA_TC_NW_256));
     static constexpr int STAGES =
-        D == 128 ? FA_TC_STAGES_128
+        D == 128 ? (VI8 ? FA_TC_STAGES_128_I8 : FA_TC_STAGES_128)
                  : (VI8 ? FA_TC_STAGES_256_I8 : (TWO256 ? FA_TC_STAGES_256_NG2 : FA_TC_STAGES_256));
     static constexpr int BOXES = D / 64;                  // 64-column boxes per row
     static constexpr int BOX_BYTES = TILE * 128;          // 16 rows x 128 B
@@ -738,7 +752,8 @@ struct Cfg {
     static constexpr int RING_BYTES = NW * WARP_BYTES;
     static constexpr int SMEM = RING_BYTES + NW * STAGES * 8 + 1024;   // + barriers + alignment
     static constexpr int CTAS_PER_SM =
-        D == 128 ? FA_TC_CTAS_128 : (VI8 ? FA_TC_CTAS_256_I8 : FA_TC_CTAS_256);
+        D == 128 ? (VI8 ? FA_TC_CTAS_128_I8 : FA_TC_CTAS_128)
+                 : (VI8 ? FA_TC_CTAS_256_I8 : FA_TC_CTAS_256);
     static_assert(CTAS_PER_SM * (SMEM + 1024) <= 228 * 1024, "shared memory per SM");
 };
 
@@ -1140,7 +1155,7 @@ __device__ __forceinline__ void column_range(const Params &p, int b, int L, int 
 // runs.
 constexpr int CL_MAX_CTAS = 8;  // the portable maximum cluster size
 template <int D, bool VI8, bool BI, int NG, bool CL = false>
-__global__ void __launch_bounds__(Cfg<D, VI8, NG>::NW * 32, 1)
+__global__ void __launch_bounds__(Cfg<D, VI8, NG>::NW * 32, Cfg<D, VI8, NG>::CTAS_PER_SM)
     fa_stream_mma_kernel(const Params p, const __grid_constant__ CUtensorMap tmK,
                          const __grid_constant__ CUtensorMap tmV)
 {
@@ -1457,38 +1472,89 @@ __global__ void __launch_bounds__(Cfg<D, VI8, NG>::NW * 32, 1)
                 constexpr int CPR = D / 16;               // 16-code chunks per row
                 const uint32_t v8 = sK + C::T_BYTES;
                 const uint32_t sc = v8 + C::V8_BYTES;
+                if constexpr (NG == 1) {
+                    // rows across lanes (lane keeps row lane % 16 in every
+                    // chunk), chunk index rotated by the row: both the int8
+                    // reads and the swizzled fp16 writes of each 8-lane phase
+                    // land in 8 different bank groups.  The loads of BAT
+                    // chunks go out before their conversions, so one shared
+                    // memory round trip serves BAT chunks.
+                    constexpr int NIT = TILE * CPR / 32;  // chunks per lane
+                    constexpr int BAT = NIT < 4 ? NIT : 4;
+                    const int row = lane % TILE;
+                    const bool live = row >= r0 && row < r1;
 #pragma unroll
-                for (int kk = 0; kk < TILE * CPR / 32; ++kk) {
-                    // rows across lanes, chunk index rotated by the row: both
-                    // the int8 reads and the swizzled fp16 writes of each
-                    // 8-lane phase land in 8 different bank groups
-                    const int q = lane + 32 * kk;
-                    const int row = q % TILE;
-                    const int cc = (q / TILE + row) % CPR;
-                    uint32_t o[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
-                    if (row >= r0 && row < r1) {
-                        uint32_t w0, w1, w2, w3;
-                        unsigned short sb;
-                        asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                                     : "=r"(w0), "=r"(w1), "=r"(w2), "=r"(w3)
-                                     : "r"(v8 + row * D + cc * 16));
-                        asm volatile("ld.shared.u16 %0, [%1];"
-                                     : "=h"(sb)
-                                     : "r"(sc + (row * (D / 32) + cc / 2) * 2));
-                        const __half2 s2 = __half2half2(__ushort_as_half(sb));
-                        dequant4(w0, s2, o[0], o[1]);
-                        dequant4(w1, s2, o[2], o[3]);
-                        dequant4(w2, s2, o[4], o[5]);
-                        dequant4(w3, s2, o[6], o[7]);
+                    for (int k0 = 0; k0 < NIT; k0 += BAT) {
+                        uint32_t w[BAT][4];
+                        unsigned short sb[BAT];
+#pragma unroll
+                        for (int j = 0; j < BAT; ++j) {
+                            const int cc = ((lane + 32 * (k0 + j)) / TILE + row) % CPR;
+                            if (live) {
+                                asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                                             : "=r"(w[j][0]), "=r"(w[j][1]), "=r"(w[j][2]),
+                                               "=r"(w[j][3])
+                                             : "r"(v8 + row * D + cc * 16));
+                                asm volatile("ld.shared.u16 %0, [%1];"
+                                             : "=h"(sb[j])
+                                             : "r"(sc + (row * (D / 32) + cc / 2) * 2));
+                            }
+                        }
+#pragma unroll
+                        for (int j = 0; j < BAT; ++j) {
+                            const int cc = ((lane + 32 * (k0 + j)) / TILE + row) % CPR;
+                            uint32_t o[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+                            if (live) {
+                                const __half2 s2 = __half2half2(__ushort_as_half(sb[j]));
+                                dequant4(w[j][0], s2, o[0], o[1]);
+                                dequant4(w[j][1], s2, o[2], o[3]);
+                                dequant4(w[j][2], s2, o[4], o[5]);
+                                dequant4(w[j][3], s2, o[6], o[7]);
+                            }
+                            asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(
+                                             swz(sV, row, 2 * cc)),
+                                         "r"(o[0]), "r"(o[1]), "r"(o[2]), "r"(o[3])
+                                         : "memory");
+                            asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(
+                                             swz(sV, row, 2 * cc + 1)),
+                                         "r"(o[4]), "r"(o[5]), "r"(o[6]), "r"(o[7])
+                                         : "memory");
+                        }
                     }
-                    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(
-                                     swz(sV, row, 2 * cc)),
-                                 "r"(o[0]), "r"(o[1]), "r"(o[2]), "r"(o[3])
-                                 : "memory");
-                    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(
-                                     swz(sV, row, 2 * cc + 1)),
-                                 "r"(o[4]), "r"(o[5]), "r"(o[6]), "r"(o[7])
-                                 : "memory");
+                } else {
+                    // two column groups hold twice the accumulators: one
+                    // chunk at a time (batched loads cost registers there and
+                    // measured 1% slower); the same chunk layout
+#pragma unroll
+                    for (int kk = 0; kk < TILE * CPR / 32; ++kk) {
+                        const int q = lane + 32 * kk;
+                        const int row = q % TILE;
+                        const int cc = (q / TILE + row) % CPR;
+                        uint32_t o[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+                        if (row >= r0 && row < r1) {
+                            uint32_t w0, w1, w2, w3;
+                            unsigned short sb;
+                            asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                                         : "=r"(w0), "=r"(w1), "=r"(w2), "=r"(w3)
+                                         : "r"(v8 + row * D + cc * 16));
+                            asm volatile("ld.shared.u16 %0, [%1];"
+                                         : "=h"(sb)
+                                         : "r"(sc + (row * (D / 32) + cc / 2) * 2));
+                            const __half2 s2 = __half2half2(__ushort_as_half(sb));
+                            dequant4(w0, s2, o[0], o[1]);
+                            dequant4(w1, s2, o[2], o[3]);
+                            dequant4(w2, s2, o[4], o[5]);
+                            dequant4(w3, s2, o[6], o[7]);
+                        }
+                        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(
+                                         swz(sV, row, 2 * cc)),
+                                     "r"(o[0]), "r"(o[1]), "r"(o[2]), "r"(o[3])
+                                     : "memory");
+                        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(
+                                         swz(sV, row, 2 * cc + 1)),
+                                     "r"(o[4]), "r"(o[5]), "r"(o[6]), "r"(o[7])
+                                     : "memory");
+                    }
                 }
                 __syncwarp();
         };
