@@ -970,11 +970,14 @@ struct Walk {
 
 // Warp-cooperative scan over the sequences: T = the flattened positions of
 // the step (tiles plus UNIT_COST per unit); when target >= 0 also the
-// sequence holding position `target` and that sequence's first position.
+// sequence holding position `target` and that sequence's first position;
+// when want >= 0 also sequence want's first position and tile count.
 // Every lane returns the same values.
 __device__ __forceinline__ long long flat_scan(const Params &p, long long target, int &b_at,
                                                long long &P_at, bool report = false,
-                                               long long *pref = nullptr)
+                                               long long *pref = nullptr, int want = -1,
+                                               long long *P_want = nullptr,
+                                               int *n_want = nullptr)
 {
     const int lane = threadIdx.x & 31;
     long long run = 0;
@@ -983,10 +986,12 @@ __device__ __forceinline__ long long flat_scan(const Params &p, long long target
     for (int b0 = 0; b0 < p.B; b0 += 32) {
         const int b = b0 + lane;
         long long c = 0;
+        int nt = 0;
         if (b < p.B) {
             int lo, hi;
             attended_range(p, b, lo, hi, report);
-            c = seq_span(p, tiles_in<TILE>(lo, hi));
+            nt = tiles_in<TILE>(lo, hi);
+            c = seq_span(p, nt);
         }
         long long x = c;
 #pragma unroll
@@ -998,6 +1003,10 @@ __device__ __forceinline__ long long flat_scan(const Params &p, long long target
         const long long excl = run + x - c;
         if (pref && b < p.B)
             pref[b] = excl;
+        if (want >= b0 && want < b0 + 32) {       // warp-uniform
+            *P_want = __shfl_sync(0xffffffffu, excl, want - b0);
+            *n_want = __shfl_sync(0xffffffffu, nt, want - b0);
+        }
         if (target >= 0 && b_at < 0) {
             const unsigned hit = __ballot_sync(0xffffffffu, b < p.B && target >= excl &&
                                                                 target < excl + c);
@@ -1958,18 +1967,22 @@ __global__ void __launch_bounds__(MERGE_THREADS) fa_stream_merge_kernel(const Pa
     const int tid = threadIdx.x;
     const int lane = tid & 31, wid = tid >> 5;
 
-    int lo, hi;
-    attended_range(p, b, lo, hi, false);
-    const int n = tiles_in<TILE>(lo, hi);
-    if (n == 0) {
-        if (tid < CH)
-            reinterpret_cast<float4 *>(p.out + row * D)[tid] = make_float4(0.f, 0.f, 0.f, 0.f);
-        return;
-    }
     const long long u = (long long)b * p.U_b + j;
     long long sb;    // workspace slot of the row's first partial
     int ns;          // partials to fold, in slot order
+    int n;           // tiles of the row's sequence
+    auto zero_row = [&] {
+        if (tid < CH)
+            reinterpret_cast<float4 *>(p.out + row * D)[tid] = make_float4(0.f, 0.f, 0.f, 0.f);
+    };
     if constexpr (BI) {
+        int lo, hi;
+        attended_range(p, b, lo, hi, false);
+        n = tiles_in<TILE>(lo, hi);
+        if (n == 0) {
+            zero_row();
+            return;
+        }
         // batch-invariant plan: the unit's chunks, one slot each
         ns = (n + p.chunk - 1) / p.chunk;
         if (ns == 1)
@@ -1977,34 +1990,35 @@ __global__ void __launch_bounds__(MERGE_THREADS) fa_stream_merge_kernel(const Pa
         asm volatile("griddepcontrol.wait;" ::: "memory");
         sb = u * p.max_chunks;
     } else {
-        // T and the flattened start of sequence b: scanned here for up to
-        // 32*SCAN_REG sequences (before the dependency wait, so it overlaps
-        // the split kernel's tail), else published by the split kernel's
-        // worker 0
+        // T, and the flattened start and tiles of sequence b: one warp's
+        // single pass over the lengths for up to 32*SCAN_REG sequences
+        // (before the dependency wait, so it overlaps the split kernel's tail
+        // where the CTA is resident by then), else published by the split
+        // kernel's worker 0
         __shared__ long long sh_T, sh_P;
+        __shared__ int sh_n;
         const bool scan_here = p.B <= 32 * SCAN_REG;
-        if (scan_here && wid == 0) {
-            int b_at;
-            long long P_at;
-            const long long T = flat_scan(p, -1, b_at, P_at);
-            long long run = 0;
-            for (int b0 = 0; b0 < b; b0 += 32) {
-                const int bb = b0 + lane;
-                long long c = 0;
-                if (bb < b) {
-                    int l2, h2;
-                    attended_range(p, bb, l2, h2, false);
-                    c = seq_span(p, tiles_in<TILE>(l2, h2));
+        if (scan_here) {
+            if (wid == 0) {
+                int b_at, nb = 0;
+                long long P_at, Pb = 0;
+                const long long T = flat_scan(p, -1, b_at, P_at, false, nullptr, b, &Pb, &nb);
+                if (lane == 0) {
+                    sh_T = T;
+                    sh_P = Pb;
+                    sh_n = nb;
                 }
-#pragma unroll
-                for (int off = 16; off >= 1; off >>= 1)
-                    c += __shfl_xor_sync(0xffffffffu, c, off);
-                run += c;
             }
-            if (lane == 0) {
-                sh_T = T;
-                sh_P = run;
-            }
+            __syncthreads();
+            n = sh_n;
+        } else {
+            int lo, hi;
+            attended_range(p, b, lo, hi, false);
+            n = tiles_in<TILE>(lo, hi);
+        }
+        if (n == 0) {                             // uniform over the CTA
+            zero_row();
+            return;
         }
         if (!scan_here) {
             asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -2012,8 +2026,8 @@ __global__ void __launch_bounds__(MERGE_THREADS) fa_stream_merge_kernel(const Pa
                 sh_T = p.pref[p.B];
                 sh_P = p.pref[b];
             }
+            __syncthreads();
         }
-        __syncthreads();
         const long long T = sh_T;
         const int We = workers_for(p, T);
         const long long us = sh_P + (long long)j * (n + UNIT_COST) + UNIT_COST;   // first tile
@@ -2160,37 +2174,27 @@ __global__ void __launch_bounds__(MERGE_ROWS_PER_CTA * 32) fa_stream_merge_rows_
     const int hh = x % p.cpu;
     float4 *dst = reinterpret_cast<float4 *>(p.out + row * D);
 
-    int lo, hi;
-    attended_range(p, b, lo, hi, false);
-    const int n = tiles_in<TILE>(lo, hi);
+    // T, and the flattened start and tiles of sequence b (as in
+    // fa_stream_merge_kernel)
+    long long T = 0, P = 0;
+    int n = 0;
+    const bool scan_here = p.B <= 32 * SCAN_REG;
+    if (scan_here) {
+        int b_at;
+        long long P_at;
+        T = flat_scan(p, -1, b_at, P_at, false, nullptr, b, &P, &n);
+    } else {
+        int lo, hi;
+        attended_range(p, b, lo, hi, false);
+        n = tiles_in<TILE>(lo, hi);
+    }
     if (n == 0) {
 #pragma unroll
         for (int c = 0; c < CPL; ++c)
             dst[lane + 32 * c] = make_float4(0.f, 0.f, 0.f, 0.f);
         return;
     }
-    // T and the flattened start of sequence b (as in fa_stream_merge_kernel)
-    long long T, P;
-    const bool scan_here = p.B <= 32 * SCAN_REG;
-    if (scan_here) {
-        int b_at;
-        long long P_at;
-        T = flat_scan(p, -1, b_at, P_at);
-        P = 0;
-        for (int b0 = 0; b0 < b; b0 += 32) {
-            const int bb = b0 + lane;
-            long long c = 0;
-            if (bb < b) {
-                int l2, h2;
-                attended_range(p, bb, l2, h2, false);
-                c = seq_span(p, tiles_in<TILE>(l2, h2));
-            }
-#pragma unroll
-            for (int off = 16; off >= 1; off >>= 1)
-                c += __shfl_xor_sync(0xffffffffu, c, off);
-            P += c;
-        }
-    } else {
+    if (!scan_here) {
         asm volatile("griddepcontrol.wait;" ::: "memory");
         T = p.pref[p.B];
         P = p.pref[b];
