@@ -1,8 +1,9 @@
 """Parity at the sizes the benchmark times for the rows beyond the plain
 decode step: multi-query decode (4 queries) and the batch-invariant plan on
 the 32 x 32K, 32/8-head, D=128 paged workload, ring decode on 64 sequences
-with 64x128-64k_d128_win's heads and lengths over 4096-row rings, and the slot
-map over a pool of 64 contiguous 16K caches.  The oracle
+with 64x128-64k_d128_win's heads and lengths over 4096-row rings, the slot
+map over a pool of 64 contiguous 16K caches, int8 V at head_dim 128 on the
+32 x 32K workload, and 8-query decode on 16x16k_d256_int8v.  The oracle
 recomputes a sample of the sequences (every output row of each), each from a
 host copy of that sequence's cache alone.
 """
@@ -145,4 +146,87 @@ def test_slot_map_eight_of_sixty_four_at_full_size():
         assert_close(got[b:b + 1], want, False, f"slot {s} (row {b}, {L} keys)")
     assert np.all(np.isfinite(got))
     del d
+    torch.cuda.empty_cache()
+
+
+def test_int8_v_head_dim_128_at_full_size():
+    """The benchmark's int8-V head_dim-128 row: 32x32k_d128_paged's shape with
+    its V packed to int8 on the GPU (3 CTAs x 4 warps per SM).  Each sampled
+    sequence's V blocks are packed again by the oracle's packer from the same
+    fp32 draw (the bytes must agree), then decoded by the oracle."""
+    wl = dataclasses.replace(WORKLOADS["32x32k_d128_paged"], name="int8v_d128", v_int8=True)
+    torch.cuda.empty_cache()
+    d = make_inputs(wl, "cuda")
+    vf = d.pop("v_f32")
+    codes = torch.empty(vf.shape, dtype=torch.int8, device="cuda")
+    scales = torch.empty(vf.shape[:-1] + (wl.head_dim // 32,), dtype=torch.float16,
+                         device="cuda")
+    binding.fa_quantize_v_int8(vf, codes, scales)
+    B, Hq, Hkv, D, P = wl.batch, wl.n_q_heads, wl.n_kv_heads, wl.head_dim, wl.page_size
+    cap = d["max_blocks"] * P
+    ws = torch.full((max(binding.fa_decode_workspace_size(B, Hq, Hkv, D, cap), 16),), 0xFF,
+                    dtype=torch.uint8, device="cuda")
+    out = torch.full((B, Hq, D), float("nan"), device="cuda")
+    binding.fa_decode(d["q"], d["k_cache"], codes, scales, d["block_table"], d["seq_lens"], Hq,
+                      Hkv, D, wl.scale, None, out, batch=B, page_size=P,
+                      max_blocks_per_seq=d["max_blocks"], num_blocks=d["num_blocks"],
+                      workspace=ws)
+    got = out.cpu().numpy()
+    assert np.all(np.isfinite(got))
+    for b in _sample(B, n=2, seed=3):
+        L = d["lens"][b]
+        nb = -(-L // P)
+        sel = d["block_table"][b, :nb].long()
+        vc, vs = oracle.pack_v_int8(vf.index_select(0, sel).cpu().numpy())
+        assert np.array_equal(codes.index_select(0, sel).cpu().numpy(), vc)
+        assert np.array_equal(scales.index_select(0, sel).cpu().numpy().view(np.uint16),
+                              vs.view(np.uint16))
+        want = oracle.decode(d["q"][b:b + 1].cpu().numpy(),
+                             d["k_cache"].index_select(0, sel).cpu().numpy(), vc, [L],
+                             scale=wl.scale, n_kv_heads=Hkv, v_scales=vs,
+                             block_table=np.arange(nb, dtype=np.int32)[None, :], page_size=P,
+                             max_blocks=nb)
+        assert_close(got[b:b + 1], want, True, f"int8 V sequence {b}")
+    del d, vf, codes, scales
+    torch.cuda.empty_cache()
+
+
+def test_multi_query_eight_queries_int8_v_at_full_size():
+    """The benchmark's int8-V multi-query row: 16x16k_d256_int8v with 8
+    queries per sequence (16 columns per KV head: two column groups per warp
+    at head_dim 256, 6 warps per CTA), V packed on the GPU and checked
+    against the oracle's packer for the sampled sequences."""
+    wl = WORKLOADS["16x16k_d256_int8v"]
+    torch.cuda.empty_cache()
+    d = make_inputs(wl, "cuda")
+    vf = d.pop("v_f32")
+    codes = torch.empty(vf.shape, dtype=torch.int8, device="cuda")
+    scales = torch.empty(vf.shape[:-1] + (wl.head_dim // 32,), dtype=torch.float16,
+                         device="cuda")
+    binding.fa_quantize_v_int8(vf, codes, scales)
+    tq = 8
+    B, Hq, Hkv, D, P = wl.batch, wl.n_q_heads, wl.n_kv_heads, wl.head_dim, wl.page_size
+    q = make_queries(wl, tq, "cuda")
+    cap = d["max_blocks"] * P
+    n = binding.fa_decode_multi_workspace_size(B, tq, Hq, Hkv, D, cap)
+    ws = torch.full((max(n, 16),), 0xFF, dtype=torch.uint8, device="cuda")
+    out = torch.full((B, tq, Hq, D), float("nan"), device="cuda")
+    binding.fa_decode_multi(q, d["k_cache"], codes, scales, d["block_table"], d["seq_lens"], Hq,
+                            Hkv, D, wl.scale, None, out, max_blocks_per_seq=d["max_blocks"],
+                            num_blocks=d["num_blocks"], workspace=ws)
+    got = out.cpu().numpy()
+    assert np.all(np.isfinite(got))
+    for b in _sample(B, n=1, seed=4):
+        L = d["lens"][b]
+        nb = -(-L // P)
+        sel = d["block_table"][b, :nb].long()
+        vc, vs = oracle.pack_v_int8(vf.index_select(0, sel).cpu().numpy())
+        assert np.array_equal(codes.index_select(0, sel).cpu().numpy(), vc)
+        want = oracle.decode_multi(q[b:b + 1].cpu().numpy(),
+                                   d["k_cache"].index_select(0, sel).cpu().numpy(), vc, [L],
+                                   scale=wl.scale, n_kv_heads=Hkv, v_scales=vs,
+                                   block_table=np.arange(nb, dtype=np.int32)[None, :],
+                                   page_size=P, max_blocks=nb)
+        assert_close(got[b:b + 1], want, True, f"int8 V multi-query sequence {b}")
+    del d, vf, codes, scales
     torch.cuda.empty_cache()
