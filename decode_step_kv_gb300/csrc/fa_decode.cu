@@ -2,9 +2,11 @@
 // for speculative verify) over a paged, contiguous or ring KV cache, for
 // sm_103a (GB300).
 //
-// One fa_decode call = two launches on the caller's stream:
+// One fa_decode call = two launches on the caller's stream (one for a small
+// step under the cluster plan, below):
 //
-//   tc::fa_stream_mma_kernel<D, int8V, BI, NG>   (the default path: BI = false)
+//   tc::fa_stream_mma_kernel<D, int8V, BI, NG, CL>   (the default path:
+//                                                      BI = false, CL = false)
 //       Persistent stream-K kernel.  The step's work is flattened into
 //       16-token tiles ordered by (sequence, KV head [x head group], tile);
 //       each warp of the grid owns an equal contiguous range of that space
@@ -12,17 +14,20 @@
 //       TMA (cp.async.bulk.tensor with the 128-byte swizzle for K and fp16 V;
 //       cp.async.bulk for int8 V and its scales).  QK and PV run on the tensor
 //       cores (mma.sync m16n8k16, fp32 accumulate) with the query heads that
-//       share the KV head (up to 8, or up to 16 in two groups of 8 at D=128:
-//       NG = 2) as the N dimension; the online softmax sits between them in
+//       share the KV head (up to 8, or up to 16 in two groups of 8: NG = 2)
+//       as the N dimension; the online softmax sits between them in
 //       registers.  At the end of each unit segment the warp writes the
 //       normalised output (it covered the whole unit) or a partial
 //       (O, m, l).  With BI (fa_decode_batch_invariant) the units
 //       are instead cut into fixed chunks that workers take whole, so a
-//       sequence's result does not depend on the rest of the batch.
+//       sequence's result does not depend on the rest of the batch.  With
+//       CL (a small step) each (sequence, KV head) unit gets one
+//       thread-block cluster whose warps split its tiles and fold their
+//       partials through distributed shared memory: no merge launch.
 //   tc::fa_stream_merge_kernel<D, BI>        log-sum-exp merge of the
-//       partials, launched with programmatic dependent launch so it is
-//       resident before the first kernel drains (tc::fa_stream_merge_rows_
-//       kernel<D>, a warp per row, when there are many rows).
+//       partials, launched with programmatic dependent launch so its CTAs
+//       start as the first kernel's leave (tc::fa_stream_merge_rows_kernel<D>,
+//       a warp per row, when there are many rows).
 //
 //   fa_split_kernel<D, GP, int8V> + fa_merge_kernel<D>   (FA_DECODE_KERNEL=simt)
 //       The CUDA-core alternative: one CTA per (split, KV head, sequence),
