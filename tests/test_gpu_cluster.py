@@ -40,6 +40,12 @@ CASES = [
     # 256 units of at most 16 tiles: one-CTA clusters, the columns folded in two passes
     (W("clusters_of_1", 32, 32, 8, 128, paged=True, window=100, window_odd_only=True, seed=41),
      [256, 1, 0, 17, 255, 128, 64, 200] * 4),
+    # int8 V at head_dim 128 runs 3 CTAs per SM, so more clusters fit at each size than with
+    # fp16 V: the same kinds of steps with int8 V, paged and contiguous
+    (W("int8_many_units", 16, 32, 8, 128, v_int8=True, paged=True, seed=42),
+     [512, 1, 300, 17, 480, 512, 0, 256, 100, 511, 64, 33, 200, 400, 16, 500]),
+    (W("int8_small_units", 32, 32, 8, 128, v_int8=True, window=50, seed=43),
+     [256, 1, 0, 17, 255, 128, 64, 200] * 4),
 ]
 
 
