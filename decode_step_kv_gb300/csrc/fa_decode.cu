@@ -3146,6 +3146,34 @@ FA_API int fa_decode_slots(const void *q, const void *k_cache, const void *v_cac
                        workspace_bytes, stream, ring != 0, 1, 0, slot_ids, n_slots);
 }
 
+// The kernel path, plan and workspace need of one call: the CUDA-core path
+// when FA_DECODE_KERNEL=simt or when the cache has 2^31 rows or more (TMA row
+// coordinates are 32-bit), else the tensor-core kernel, which alone has the
+// per-column query ranges of several queries and the chunk plan.
+static int call_plan(int batch, int n_q_heads, int n_kv_heads, int D, long long cap, bool vi8,
+                     bool ring, int tq, int chunk, long long kv_rows_total, int *sms, Plan *pl,
+                     size_t *need)
+{
+    const int rc = device_sms(sms);
+    if (rc)
+        return rc;
+    Path path = choose_path();
+    if (kv_rows_total >= (1ll << 31)) {
+        if (tq > 1 || chunk > 0)
+            return fail(FA_ERR_LAYOUT, "fa_decode: caches of 2^31 rows or more are not "
+                                       "supported with several queries or batch-invariant "
+                                       "splits");
+        path = Path::Simt;
+    }
+    if (tq > 1 || chunk > 0)
+        path = Path::Mma;
+    // a ring's attended range (the last cap tokens) can straddle one more tile
+    *pl = make_plan(path, batch, n_q_heads, n_kv_heads, D, ring ? cap + 16 : cap, *sms, vi8, tq,
+                    chunk);
+    *need = plan_workspace(*pl, batch, n_q_heads, D);
+    return 0;
+}
+
 static int decode_impl(const void *q, const void *k_cache, const void *v_cache,
                        const void *v_scales, const int32_t *block_table,
                        const int32_t *seq_lens, int n_q_heads, int n_kv_heads, int head_dim,
@@ -3214,27 +3242,15 @@ static int decode_impl(const void *q, const void *k_cache, const void *v_cache,
         return fail(FA_ERR_ALIAS, "fa_decode: out overlaps an input or the workspace");
     if (batch == 0)
         return 0;
-    int sms = 0;
-    int rc = device_sms(&sms);
-    if (rc)
-        return rc;
-    Path path = choose_path();
     const long long kv_rows_total = paged ? (long long)num_blocks * n_kv_heads * page_size
                                           : slots * n_kv_heads * cap;
-    if (kv_rows_total >= (1ll << 31)) {
-        if (tq > 1 || chunk > 0)
-            return fail(FA_ERR_LAYOUT, "fa_decode: caches of 2^31 rows or more are not "
-                                       "supported with several queries or batch-invariant "
-                                       "splits");
-        path = Path::Simt;   // TMA row coordinates are 32-bit
-    }
-    if (tq > 1 || chunk > 0)
-        path = Path::Mma;    // only the tensor-core kernel has per-column query ranges and
-                             // the chunk plan
-    // a ring's attended range (the last cap tokens) can straddle one more tile
-    const Plan pl = make_plan(path, batch, n_q_heads, n_kv_heads, D, ring ? cap + 16 : cap, sms,
-                              vi8, tq, chunk);
-    const size_t need = plan_workspace(pl, batch, n_q_heads, D);
+    int sms = 0;
+    Plan pl;
+    size_t need = 0;
+    int rc = call_plan(batch, n_q_heads, n_kv_heads, D, cap, vi8, ring, tq, chunk,
+                       kv_rows_total, &sms, &pl, &need);
+    if (rc)
+        return rc;
     if (need == WS_OVERFLOW)
         return fail(FA_ERR_WORKSPACE, "fa_decode: the workspace for these sizes exceeds 2^64 bytes");
     if (need > 0 && (!workspace || workspace_bytes < need))
@@ -3654,8 +3670,17 @@ FA_API int fa_decode_noalloc(const void *q, const void *k_cache, const void *v_c
                                       : (long long)max_blocks_per_seq;
     if (cap > (1ll << 30))
         return fail(FA_ERR_LAYOUT, "fa_decode_noalloc: capacity %lld tokens too large", cap);
-    const size_t need = fa_decode_workspace_size(batch, n_q_heads, n_kv_heads, head_dim,
-                                                 (int)cap, 0);
+    // the scratch this call needs: its own V type and the plan fa_decode takes
+    const long long kv_rows_total =
+        block_table ? (long long)(num_blocks > 0 ? num_blocks : 0) * n_kv_heads * page_size
+                    : (long long)batch * n_kv_heads * cap;
+    int sms = 0;
+    Plan pl;
+    size_t need = 0;
+    const int prc = call_plan(batch, n_q_heads, n_kv_heads, head_dim, cap, v_scales != nullptr,
+                              false, 1, 0, kv_rows_total, &sms, &pl, &need);
+    if (prc)
+        return prc;
     if (need > FA_NOALLOC_SCRATCH_BYTES)
         return fail(FA_ERR_WORKSPACE,
                     "fa_decode_noalloc: these sizes need %zu bytes of scratch, more than the "

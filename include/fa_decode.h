@@ -398,9 +398,10 @@ FA_API int fa_decode_device_status(unsigned int *status, void *stream);
  * It allocates nothing and calls no allocating routine.
  *
  * Limits and rules:
- *   - sizes whose scratch need (fa_decode_workspace_size) exceeds
- *     FA_NOALLOC_SCRATCH_BYTES are rejected with FA_ERR_WORKSPACE and a
- *     message stating both sizes; nothing is launched;
+ *   - a call whose own scratch need (the workspace fa_decode takes for these
+ *     sizes and this V type; fa_decode_workspace_size, which covers both V
+ *     types, bounds it) exceeds FA_NOALLOC_SCRATCH_BYTES is rejected with
+ *     FA_ERR_WORKSPACE and a message stating both sizes; nothing is launched;
  *   - the first call in a CUDA context (for runtime-API callers: the first
  *     call on a device) looks up the array's device address in that context,
  *     with it current, and caches it under the context's id; make that
